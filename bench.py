@@ -1,0 +1,391 @@
+"""Benchmark of the fused MLA hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--quick]
+
+One step = one pass of the hot path over one batch of synthetic input: the causal
+bf16 MLA prefill B=4 H=128 S=4096 (the headline ``value``, TFLOP/s) followed by the
+absorbed bf16 decode B=64 H=128 L=4096 (reported under ``decode``, KV GB/s).  The fp8
+per-token-scale prefill (B=2 H=128 S=8192) and the ragged fp8 decode (B=128 H=16
+q_len=2) are timed the same way and reported under ``prefill_fp8`` / ``decode_fp8``.
+Inputs are seeded synthetic tensors (numpy PCG64), resident in HBM before timing.
+
+``--impl reference`` times the fp64 CPU oracle instead, on bounded samples of the
+same prefill workload, and prints the same JSON line with ``"impl": "reference"``.
+With N > 1 (torchrun) every rank runs an independent replica (no collective on the
+data path): ``value`` = work of all ranks / max over ranks of the elapsed time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("MLA prefill TFLOP/s (% tensor peak); MLA decode KV GB/s (% of HBM peak), 1 GB300")
+HEADLINE = "prefill_b4h128s4096_bf16"
+DECODE = "decode_b64h128t1l4096_bf16"
+PREFILL_FP8 = "prefill_b2h128s8192_fp8"
+DECODE_FP8 = "decode_b128h16t2_ragged_fp8"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def prefill_flops(B, H, S, dqk=192, dv=128, causal=True):
+    pairs = S * (S + 1) // 2 if causal else S * S
+    return 2.0 * B * H * pairs * (dqk + dv)
+
+
+def decode_kv_bytes(inp):
+    per = (inp.d_latent + inp.d_rope) * (1 if inp.fp8 else 2) + (4 if inp.fp8 else 0)
+    return float(inp.cache_lens.astype("int64").sum()) * per
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, "mla_flash_attention_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(key, src_files):
+    """Per-launch DRAM bytes from the committed ncu summary, if taken on this kernel source."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(key)
+    if not d or d.get("src_sha") != kernel_source_hash(src_files):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", "mla_clocks_%d_%d.csv" % (os.getpid(), gpu_index))
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+def time_calls(fn, steps, warmup, flush=None):
+    """Per-call CUDA-event times (ms) on the current stream; L2 flush between calls if given."""
+    import torch
+
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(steps):
+        if flush is not None:
+            flush()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        fn()
+        e.record()
+        evs.append((s, e))
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in evs]
+
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    from gen import config_inputs
+    from mla_flash_attention_gb300 import binding
+    from mla_flash_attention_gb300.testing import decode_to_device, prefill_to_device
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x):
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    pk = peaks()
+    flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush():
+        flush_buf.zero_()
+
+    # ---------------- headline: bf16 prefill
+    inp = config_inputs(HEADLINE)
+    t = prefill_to_device(inp, dev)
+    flops = prefill_flops(inp.B, inp.H, inp.S)
+
+    def call_prefill():
+        binding.mla_prefill(*t["args"], softmax_scale=inp.softmax_scale, causal=True)
+
+    barrier()
+    with ClockSampler(local) as clk:
+        ms = time_calls(call_prefill, args.steps, args.warmup)
+    barrier()
+    ms_mean = max_over_ranks(sum(ms) / len(ms))
+    clocks = clk.summary()
+    launches = args.steps * 1
+
+    # end to end through the C ABI with host buffers (pinned): H2D inputs, call, D2H outputs
+    host = prefill_to_device(inp, dev, pin=True)
+    dev_in = [None if x is None else torch.empty_like(x, device=dev) for x in host["args"]]
+    out_h = torch.empty((inp.B, inp.S, inp.H, inp.d_v), dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty((inp.B, inp.H, inp.S), dtype=torch.float32).pin_memory()
+    out_d = torch.empty_like(out_h, device=dev)
+    lse_d = torch.empty_like(lse_h, device=dev)
+    h2d = sum(x.numel() * x.element_size() for x in host["args"] if x is not None)
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+
+    def call_e2e():
+        for d_, h_ in zip(dev_in, host["args"]):
+            if d_ is not None:
+                d_.copy_(h_, non_blocking=True)
+        binding.mla_prefill(*dev_in, softmax_scale=inp.softmax_scale, causal=True, out=out_d,
+                            lse=lse_d)
+        out_h.copy_(out_d, non_blocking=True)
+        lse_h.copy_(lse_d, non_blocking=True)
+
+    e2e_ms = max_over_ranks(statistics.mean(time_calls(call_e2e, max(2, args.steps // 2), 1)))
+    launches += max(2, args.steps // 2) + 1  # e2e calls are outside the kernel-timed region
+    del host, dev_in, out_d, lse_d, t
+    torch.cuda.empty_cache()
+
+    res = {
+        "metric": METRIC, "value": world * flops / (ms_mean * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_mean,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded PCG64 N(0,1) rounded to bf16 (no dataset)",
+        "config": {"workload": HEADLINE, "B": inp.B, "H": inp.H, "S": inp.S, "d_nope": 128,
+                   "d_rope": 64, "d_v": 128, "causal": True, "softmax_scale": inp.softmax_scale,
+                   "l2": "inputs (1.6 GB) larger than L2; no flush",
+                   "parallelism": "replicas (dp%d, no collective)" % world},
+    }
+    src = ["prefill_simt.cu"]
+    achieved = flops / (ms_mean * 1e-3) / 1e12
+    res["roofline"] = {"kernel": "prefill", "bound": "tensor", "achieved": achieved,
+                       "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                       "frac": achieved / pk["bf16_tflops"],
+                       "traffic": recorded_traffic("prefill_bf16", src),
+                       "peak_source": pk["source"] + " (bf16 dense, burst; of measured)"}
+    res["e2e"] = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+    res["clocks"] = clocks
+
+    # ---------------- decode (bf16) and the fp8 workloads
+    def decode_entry(name):
+        dinp = config_inputs(name)
+        d = decode_to_device(dinp, dev)
+        ws = torch.empty(binding.decode_workspace_size(dinp.B, dinp.H, dinp.T), dtype=torch.uint8,
+                         device=dev)
+        out = torch.empty((dinp.B, dinp.T, dinp.H, dinp.d_latent), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((dinp.B, dinp.H, dinp.T), dtype=torch.float32, device=dev)
+
+        def call():
+            binding.mla_decode(*d["args"], **d["kwargs"], softmax_scale=dinp.softmax_scale,
+                               causal=True, out=out, lse=lse, workspace=ws)
+
+        barrier()
+        dms = max_over_ranks(statistics.mean(time_calls(call, args.steps, args.warmup, flush)))
+        kv = decode_kv_bytes(dinp)
+        gbs = kv / (dms * 1e-3) / 1e9
+        binding.check_device_error()
+        return {"workload": name, "ms": dms, "kv_bytes": kv, "kv_gbs": world * gbs,
+                "frac_hbm": gbs / pk["hbm_gbs"], "l2": "flushed (256 MB write) before each call",
+                "launches_per_call": 2}
+
+    def prefill_entry(name):
+        pinp = config_inputs(name)
+        pt = prefill_to_device(pinp, dev)
+
+        def call():
+            binding.mla_prefill(*pt["args"], softmax_scale=pinp.softmax_scale, causal=True)
+
+        barrier()
+        pms = max_over_ranks(statistics.mean(time_calls(call, args.steps, args.warmup)))
+        f = prefill_flops(pinp.B, pinp.H, pinp.S)
+        tf = f / (pms * 1e-3) / 1e12
+        return {"workload": name, "ms": pms, "flops": f, "tflops": world * tf,
+                "frac_bf16_peak": tf / pk["bf16_tflops"], "out_dtype": "fp32"}
+
+    res["decode"] = decode_entry(DECODE)
+    launches += args.steps * 2
+    if not args.quick:
+        res["prefill_fp8"] = prefill_entry(PREFILL_FP8)
+        res["decode_fp8"] = decode_entry(DECODE_FP8)
+        launches += args.steps * 3
+    res["gpu_launches"] = launches
+    if rank == 0:
+        res["cpu_baseline"] = cpu_baseline(inp_name=HEADLINE, budget_s=args.cpu_seconds)
+        print(json.dumps(res))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# --------------------------------------------------------------------------- CPU oracle
+
+def _cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(inp_name=HEADLINE, budget_s=15.0, inp=None):
+    """Time the fp64 oracle on (batch, head) slices of the prefill workload for ~budget_s."""
+    import numpy as np
+
+    import oracle
+    from gen import CONFIGS, make_prefill
+
+    c = CONFIGS[inp_name]
+    if inp is None:
+        # one (batch, head) slice of the workload's shape: same S, depths and distribution
+        inp = make_prefill(1, 1, c["S"], fp8=c["fp8"], seed=c["seed"])
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        oracle.prefill_bh(inp, 0, 0)
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    f = n * prefill_flops(1, 1, inp.S)
+    return {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": _cpu_cores(), "kind": "oracle",
+            "sample": "%d x one (batch, head) slice S=%d of %s (%.1f s, numpy fp64)" % (
+                n, inp.S, inp_name, dt)}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from gen import CONFIGS, make_prefill
+
+    c = CONFIGS[HEADLINE]
+    inp = make_prefill(1, 1, c["S"], seed=c["seed"])
+    import oracle
+
+    for _ in range(args.warmup):
+        oracle.prefill_bh(inp, 0, 0, rows=range(0, c["S"], 64))
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.prefill_bh(inp, 0, 0)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * statistics.mean(times)
+    f = prefill_flops(1, 1, c["S"])
+    v = f / (ms * 1e-3) / 1e12
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    res = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s",
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic: seeded PCG64 N(0,1) rounded to bf16 (no dataset)",
+           "config": {"workload": HEADLINE, "B": c["B"], "H": c["H"], "S": c["S"],
+                      "sample": "one (batch, head) slice per step"},
+           "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": _cpu_cores(),
+                            "kind": "oracle",
+                            "sample": "one (batch, head) slice S=%d per step, numpy fp64" % c["S"]},
+           "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0},
+           "gpu_launches": 0}
+    print(json.dumps(res))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--quick", action="store_true", help="headline prefill + bf16 decode only")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.impl == "ours":
+        args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,140 @@
+/*
+ * mla.h -- C ABI of the GB300 (sm_103a) fused multi-head latent attention library.
+ *
+ * Two operations, both exact attention in flash form (scores S = Q K', online
+ * softmax, O += P V -- Modular API docs, "KVPipelineGeneric" (nn/attention/gpu/
+ * nvidia/sm100/mla_decode_utils), struct description and Parameters):
+ *
+ *   mla_prefill  causal (or full) self-attention over split nope+rope head depths,
+ *                optionally with fp8 e4m3 Q_nope/K_nope/V and one fp32 scale per
+ *                query and per key token ("MLASmemStorage" of nn/attention/gpu/
+ *                nvidia/sm100/mla_prefill_per_token_scale: Fields q_smem, kv_smem,
+ *                q_scale_smem, k_scale_smem).
+ *   mla_decode   absorbed decode: T new query tokens per sequence attend to one
+ *                shared latent head (d_latent + d_rope columns per token) kept in a
+ *                paged cache; V is the first d_latent columns of the same rows.
+ *                Split over the key axis across CTAs, then merged by log-sum-exp.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor arguments are DEVICE pointers, contiguous, innermost dimension
+ *     last, 16-byte aligned.  The caller owns every buffer (including the decode
+ *     workspace); the library allocates no device memory and keeps no pointer
+ *     after a call returns.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  Inputs are only read; `out` and `lse` are written in full.
+ *   - Argument errors are detected on the host before any launch and return a
+ *     non-zero mla_status with nothing launched; mla_last_error() then returns a
+ *     message (thread-local, valid until the next call on the same thread).
+ *   - A launch failure returns MLA_ERR_CUDA.  Errors found by the device itself
+ *     (a bounded pipeline wait that ran out) are latched in a device word and
+ *     reported by mla_check_device_error().
+ *   - No C++ exception crosses this boundary.
+ *
+ * Softmax scale and LSE: the score of query row i and key j is
+ *   s_ij = softmax_scale * (q_nope_i . k_nope_j + q_rope_i . k_rope_j)
+ * (fp8: q_nope_i scaled by q_scale_i, k_nope_j by k_scale_j); LSE_i is the natural
+ * log of sum_j exp(s_ij) over the keys row i may see, stored as fp32.  A row that
+ * sees no key gets O = 0 and LSE = -inf.
+ */
+#ifndef MLA_GB300_H_
+#define MLA_GB300_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,  /* null pointer, negative/zero size, misalignment */
+  MLA_ERR_UNSUPPORTED = 2,  /* valid but not built: head depths, dtypes, page size */
+  MLA_ERR_WORKSPACE = 3,    /* decode workspace missing or too small */
+  MLA_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed */
+  MLA_ERR_TIMEOUT = 5,      /* a device-side bounded wait ran out (device word) */
+  MLA_ERR_DEVICE_CHECK = 6  /* a device-side bounds check failed (device word) */
+} mla_status;
+
+typedef enum {
+  MLA_BF16 = 0,
+  MLA_FP8_E4M3 = 1,
+  MLA_FP32 = 2
+} mla_dtype;
+
+/*
+ * mla_prefill -- O = softmax(S) V per (batch, head), S as above.
+ *
+ * Layouts (element type in brackets):
+ *   q_nope  [B, S, H, d_nope]  (qkv_dtype)      q_rope [B, S, H, d_rope] (bf16)
+ *   k_nope  [B, S, H, d_nope]  (qkv_dtype)      k_rope [B, S, d_rope]    (bf16)
+ *           one rope key per token, shared by all H heads
+ *   v       [B, S, H, d_v]     (qkv_dtype)
+ *   q_scale [B, S] fp32, k_scale [B, S] fp32 -- required iff qkv_dtype is
+ *           MLA_FP8_E4M3 (then k_scale also dequantises V), must be NULL for bf16
+ *   out     [B, S, H, d_v]     (out_dtype: MLA_BF16, or MLA_FP32)
+ *   lse     [B, H, S] fp32
+ * causal != 0: query i sees keys 0..i (square problem).  causal == 0: all keys.
+ * Supported: d_nope = 128, d_rope = 64, d_v = 128; qkv_dtype MLA_BF16 or
+ * MLA_FP8_E4M3; S >= 1; B*H*S*max(d) < 2^31 per tensor dimension product.
+ */
+mla_status mla_prefill(const void* q_nope, const void* q_rope, const void* k_nope,
+                       const void* k_rope, const void* v, const float* q_scale,
+                       const float* k_scale, void* out, float* lse, int B, int H, int S,
+                       int d_nope, int d_rope, int d_v, float softmax_scale, int causal,
+                       mla_dtype qkv_dtype, mla_dtype out_dtype, void* stream);
+
+/*
+ * mla_decode_workspace_size -- bytes of device workspace mla_decode needs for a
+ * batch of B sequences with H heads and q_len new tokens each.  Independent of
+ * the cache lengths (the split plan is sized for its worst case).
+ */
+size_t mla_decode_workspace_size(int B, int H, int q_len, int d_latent);
+
+/*
+ * mla_decode -- absorbed MLA decode over a paged latent cache.
+ *
+ *   q_latent   [B, q_len, H, d_latent] bf16     q_rope [B, q_len, H, d_rope] bf16
+ *   kv_cache   [num_pages, page_size, d_latent + d_rope]  (kv_dtype: bf16 or e4m3)
+ *   kv_scale   [num_pages, page_size] fp32 -- one scale per cache row; required iff
+ *              kv_dtype is MLA_FP8_E4M3, must be NULL for bf16
+ *   page_table [B, max_pages_per_seq] int32 -- token j of sequence b is row
+ *              j % page_size of page page_table[b][j / page_size]; entries past
+ *              the sequence's last page are never read
+ *   cache_lens [B] int32 -- L_b, counting the q_len new tokens, which occupy
+ *              positions L_b - q_len .. L_b - 1 (0 <= L_b <= max_pages*page_size)
+ *   out        [B, q_len, H, d_latent] bf16
+ *   lse        [B, H, q_len] fp32
+ *   workspace  device buffer of at least mla_decode_workspace_size() bytes
+ * causal != 0: new token t sees keys 0 .. L_b - q_len + t; causal == 0: keys
+ * 0 .. L_b - 1.  Cache rows past L_b may hold anything (even NaN): they are
+ * never mixed into a result.  Page indices must lie in [0, num_pages): entries
+ * outside are reported through MLA_ERR_DEVICE_CHECK (that page is skipped).
+ * Supported: d_latent = 512, d_rope = 64, page_size = 64, q_len * H <= 128.
+ */
+mla_status mla_decode(const void* q_latent, const void* q_rope, const void* kv_cache,
+                      const float* kv_scale, const int* page_table, const int* cache_lens,
+                      void* out, float* lse, int B, int H, int q_len, int d_latent,
+                      int d_rope, int page_size, int max_pages_per_seq, int num_pages,
+                      float softmax_scale, int causal, mla_dtype kv_dtype, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/*
+ * mla_check_device_error -- synchronise `stream`, then read and clear the device
+ * error word latched by earlier kernels of this library on the current device.
+ * Returns MLA_OK, MLA_ERR_TIMEOUT or MLA_ERR_DEVICE_CHECK (or MLA_ERR_CUDA if the
+ * synchronisation itself failed).
+ */
+mla_status mla_check_device_error(void* stream);
+
+/* Message describing the last non-OK status returned on this thread. */
+const char* mla_last_error(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int mla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_GB300_H_ */

@@ -1,0 +1,182 @@
+"""Thin ctypes binding of the C ABI (include/mla.h).
+
+Argument marshalling only: torch tensors are checked for device, dtype, shape and
+contiguity, then their device pointers and the current CUDA stream are passed to
+the library.  Every step of the attention runs inside the library's CUDA kernels;
+there is no fallback of any kind: if the shared library is missing, importing this
+module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmla_gb300.so")
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(
+        "libmla_gb300.so is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+_lib = ctypes.CDLL(_LIB_PATH)
+
+MLA_OK = 0
+MLA_BF16, MLA_FP8_E4M3, MLA_FP32 = 0, 1, 2
+STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED", 3: "MLA_ERR_WORKSPACE",
+          4: "MLA_ERR_CUDA", 5: "MLA_ERR_TIMEOUT", 6: "MLA_ERR_DEVICE_CHECK"}
+
+_vp, _fp, _ip = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
+_i, _f, _sz = ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+
+_lib.mla_prefill.restype = _i
+_lib.mla_prefill.argtypes = [_vp, _vp, _vp, _vp, _vp, _fp, _fp, _vp, _fp, _i, _i, _i, _i, _i, _i,
+                             _f, _i, _i, _i, _vp]
+_lib.mla_decode_workspace_size.restype = _sz
+_lib.mla_decode_workspace_size.argtypes = [_i, _i, _i, _i]
+_lib.mla_decode.restype = _i
+_lib.mla_decode.argtypes = [_vp, _vp, _vp, _fp, _ip, _ip, _vp, _fp, _i, _i, _i, _i, _i, _i, _i, _i,
+                            _f, _i, _i, _vp, _sz, _vp]
+_lib.mla_check_device_error.restype = _i
+_lib.mla_check_device_error.argtypes = [_vp]
+_lib.mla_last_error.restype = ctypes.c_char_p
+_lib.mla_last_error.argtypes = []
+_lib.mla_version.restype = _i
+_lib.mla_version.argtypes = []
+
+EXPORTED = ("mla_prefill", "mla_decode_workspace_size", "mla_decode", "mla_check_device_error",
+            "mla_last_error", "mla_version")
+
+
+class MLAError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__("%s: %s" % (STATUS.get(status, status), msg))
+        self.status = status
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def raw():
+    """The ctypes library handle (for tests that exercise the C ABI directly)."""
+    return _lib
+
+
+def _check(st: int):
+    if st != MLA_OK:
+        raise MLAError(st, _lib.mla_last_error().decode(errors="replace"))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, name, dtype, shape):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must have dtype %s (got %s)" % (name, dtype, t.dtype))
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s (got %s)" % (name, tuple(shape), tuple(t.shape)))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def version() -> int:
+    return _lib.mla_version()
+
+
+def check_device_error(stream=None) -> None:
+    _check(_lib.mla_check_device_error(_stream(stream)))
+
+
+def mla_prefill(q_nope, q_rope, k_nope, k_rope, v, q_scale=None, k_scale=None, *,
+                softmax_scale: float, causal: bool = True, out=None, lse=None,
+                out_dtype=None, stream=None):
+    """Fused MLA prefill.  Returns (out [B,S,H,d_v], lse [B,H,S] fp32).
+
+    bf16 inputs: q_nope/k_nope/v bf16.  fp8 inputs: q_nope/k_nope/v float8_e4m3fn with
+    q_scale/k_scale fp32 [B,S].  Rope parts are always bf16 (k_rope [B,S,d_rope]).
+    """
+    B, S, H, dn = q_nope.shape
+    dr = q_rope.shape[-1]
+    dv = v.shape[-1]
+    fp8 = q_nope.dtype == torch.float8_e4m3fn
+    qkv_dt = torch.float8_e4m3fn if fp8 else torch.bfloat16
+    _need(q_nope, "q_nope", qkv_dt, (B, S, H, dn))
+    _need(q_rope, "q_rope", torch.bfloat16, (B, S, H, dr))
+    _need(k_nope, "k_nope", qkv_dt, (B, S, H, dn))
+    _need(k_rope, "k_rope", torch.bfloat16, (B, S, dr))
+    _need(v, "v", qkv_dt, (B, S, H, dv))
+    if fp8:
+        _need(q_scale, "q_scale", torch.float32, (B, S))
+        _need(k_scale, "k_scale", torch.float32, (B, S))
+    elif q_scale is not None or k_scale is not None:
+        raise ValueError("q_scale/k_scale are only used with fp8 inputs")
+    if out_dtype is None:
+        out_dtype = torch.float32 if fp8 else torch.bfloat16
+    dev = q_nope.device
+    if out is None:
+        out = torch.empty((B, S, H, dv), dtype=out_dtype, device=dev)
+    if lse is None:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+    _need(out, "out", out_dtype, (B, S, H, dv))
+    _need(lse, "lse", torch.float32, (B, H, S))
+    st = _lib.mla_prefill(_ptr(q_nope), _ptr(q_rope), _ptr(k_nope), _ptr(k_rope), _ptr(v),
+                          _ptr(q_scale), _ptr(k_scale), _ptr(out), _ptr(lse), B, H, S, dn, dr,
+                          dv, float(softmax_scale), int(bool(causal)),
+                          MLA_FP8_E4M3 if fp8 else MLA_BF16,
+                          MLA_FP32 if out_dtype == torch.float32 else MLA_BF16, _stream(stream))
+    _check(st)
+    return out, lse
+
+
+def decode_workspace_size(B: int, H: int, q_len: int, d_latent: int = 512) -> int:
+    return int(_lib.mla_decode_workspace_size(B, H, q_len, d_latent))
+
+
+def mla_decode(q_latent, q_rope, kv_cache, page_table, cache_lens, kv_scale=None, *,
+               softmax_scale: float, causal: bool = True, out=None, lse=None, workspace=None,
+               stream=None):
+    """Absorbed MLA decode over a paged latent cache.  Returns (out [B,T,H,dl] bf16,
+    lse [B,H,T] fp32).  kv_cache bf16 or float8_e4m3fn [num_pages, page_size, dl+dr];
+    kv_scale fp32 [num_pages, page_size] for fp8."""
+    B, T, H, dl = q_latent.shape
+    dr = q_rope.shape[-1]
+    num_pages, page_size, D = kv_cache.shape
+    fp8 = kv_cache.dtype == torch.float8_e4m3fn
+    _need(q_latent, "q_latent", torch.bfloat16, (B, T, H, dl))
+    _need(q_rope, "q_rope", torch.bfloat16, (B, T, H, dr))
+    _need(kv_cache, "kv_cache", torch.float8_e4m3fn if fp8 else torch.bfloat16,
+          (num_pages, page_size, dl + dr))
+    if fp8:
+        _need(kv_scale, "kv_scale", torch.float32, (num_pages, page_size))
+    elif kv_scale is not None:
+        raise ValueError("kv_scale is only used with an fp8 cache")
+    max_pages = page_table.shape[1]
+    _need(page_table, "page_table", torch.int32, (B, max_pages))
+    _need(cache_lens, "cache_lens", torch.int32, (B,))
+    dev = q_latent.device
+    if out is None:
+        out = torch.empty((B, T, H, dl), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.bfloat16, (B, T, H, dl))
+    _need(lse, "lse", torch.float32, (B, H, T))
+    need = decode_workspace_size(B, H, T, dl)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    st = _lib.mla_decode(_ptr(q_latent), _ptr(q_rope), _ptr(kv_cache), _ptr(kv_scale),
+                         _ptr(page_table), _ptr(cache_lens), _ptr(out), _ptr(lse), B, H, T, dl,
+                         dr, page_size, max_pages, num_pages, float(softmax_scale),
+                         int(bool(causal)), MLA_FP8_E4M3 if fp8 else MLA_BF16, _ptr(workspace),
+                         workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st)
+    return out, lse

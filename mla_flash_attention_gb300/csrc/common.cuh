@@ -1,0 +1,62 @@
+// Shared device helpers of the GB300 MLA library (CUDA path only).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mla {
+
+// Device error word bits (latched with atomicOr, read and cleared by the host).
+enum : unsigned int {
+  kErrTimeout = 1u,     // a bounded mbarrier / flag wait ran out
+  kErrBadPage = 2u,     // a page-table entry outside [0, num_pages)
+};
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t bits) {
+  return __uint_as_float(static_cast<uint32_t>(bits) << 16);
+}
+
+__device__ __forceinline__ float e4m3_to_f32(uint8_t code) {
+  __nv_fp8_e4m3 v;
+  v.__x = code;
+  return static_cast<float>(v);
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rne(float x) {
+  __nv_bfloat16 h = __float2bfloat16_rn(x);
+  return *reinterpret_cast<uint16_t*>(&h);
+}
+
+__device__ __forceinline__ void latch_error(unsigned int* err, unsigned int bits) {
+  if (err) atomicOr(err, bits);
+}
+
+// Number of cache pages of a sequence of length L.
+__device__ __forceinline__ int pages_of(int L, int page_size) {
+  return L > 0 ? (L + page_size - 1) / page_size : 0;
+}
+
+// Split plan of the decode key axis (computed identically by every CTA that needs
+// it, from cache_lens alone): the pages of all sequences are numbered in sequence
+// order (sequence b owns flat pages [P_b, P_b + n_b)), and work CTA c of G takes flat
+// pages [c*chunk, (c+1)*chunk) with chunk = ceil(total / G).  The partial result of
+// CTA c for sequence b goes to slot c + b, which is unique because consecutive CTAs
+// never move backwards through the sequences; there are at most G + B - 1 slots.
+struct SplitPlan {
+  int total;  // pages over all sequences
+  int chunk;  // pages per work CTA
+};
+
+__device__ __forceinline__ SplitPlan make_split_plan(const int* cache_lens, int B,
+                                                     int page_size, int G) {
+  int total = 0;
+  for (int b = 0; b < B; ++b) total += pages_of(__ldg(cache_lens + b), page_size);
+  SplitPlan p;
+  p.total = total;
+  p.chunk = total > 0 ? (total + G - 1) / G : 1;
+  return p;
+}
+
+}  // namespace mla

@@ -1,0 +1,217 @@
+// Host side of the C ABI declared in include/mla.h: argument validation, the
+// device error word, decode workspace sizing and kernel dispatch.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "../../include/mla.h"
+#include "common.cuh"
+
+namespace mla {
+cudaError_t launch_prefill_simt(const void* q_nope, const void* q_rope, const void* k_nope,
+                                const void* k_rope, const void* v, const float* q_scale,
+                                const float* k_scale, void* out, float* lse, int B, int H,
+                                int S, float softmax_scale, int causal, bool fp8, bool out_f32,
+                                cudaStream_t stream);
+cudaError_t launch_prefill_sm103_bf16(const void* q_nope, const void* q_rope, const void* k_nope,
+                                      const void* k_rope, const void* v, void* out, float* lse,
+                                      int B, int H, int S, float softmax_scale, int causal,
+                                      bool out_f32, unsigned int* err, cudaStream_t stream);
+cudaError_t launch_decode_simt(const void* q_latent, const void* q_rope, const void* kv_cache,
+                               const float* kv_scale, const int* page_table,
+                               const int* cache_lens, void* out, float* lse, int B, int H,
+                               int T, int max_pages, int num_pages, float softmax_scale,
+                               int causal, bool fp8, float* part_o, float* part_lse, int G,
+                               unsigned int* err, cudaStream_t stream);
+}  // namespace mla
+
+namespace {
+
+thread_local std::string g_last_error;
+
+__device__ unsigned int g_device_error = 0;
+
+mla_status fail(mla_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+mla_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(MLA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Address of the device error word on the current device (looked up once per device).
+unsigned int* device_error_word() {
+  static unsigned int* cache[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!cache[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<unsigned int*>(p);
+  }
+  return cache[dev];
+}
+
+int num_sms_current() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+constexpr int kDecodeCtasPerSm = 1;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct DecodeWorkspace {
+  float* part_o;
+  float* part_lse;
+  size_t bytes;
+};
+
+DecodeWorkspace decode_workspace_layout(void* base, int B, int TH, int d_latent, int G) {
+  DecodeWorkspace w;
+  const size_t slots = (size_t)G + (size_t)B;
+  const size_t o_bytes = align_up(slots * TH * d_latent * sizeof(float), 256);
+  const size_t l_bytes = align_up(slots * TH * sizeof(float), 256);
+  w.part_o = static_cast<float*>(base);
+  w.part_lse = reinterpret_cast<float*>(static_cast<char*>(base) + o_bytes);
+  w.bytes = o_bytes + l_bytes;
+  return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_last_error(void) { return g_last_error.c_str(); }
+
+int mla_version(void) { return 100; }
+
+mla_status mla_check_device_error(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned int* w = device_error_word();
+  if (!w) return fail(MLA_ERR_CUDA, "device error word not reachable");
+  unsigned int v = 0;
+  e = cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  const unsigned int zero = 0;
+  e = cudaMemcpy(w, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+  if (v & mla::kErrTimeout) return fail(MLA_ERR_TIMEOUT, "a device-side pipeline wait timed out (word 0x%x)", v);
+  if (v & mla::kErrBadPage)
+    return fail(MLA_ERR_DEVICE_CHECK, "a page-table entry or cache length was out of range (word 0x%x)", v);
+  return MLA_OK;
+}
+
+mla_status mla_prefill(const void* q_nope, const void* q_rope, const void* k_nope,
+                       const void* k_rope, const void* v, const float* q_scale,
+                       const float* k_scale, void* out, float* lse, int B, int H, int S,
+                       int d_nope, int d_rope, int d_v, float softmax_scale, int causal,
+                       mla_dtype qkv_dtype, mla_dtype out_dtype, void* stream) {
+  if (!q_nope || !q_rope || !k_nope || !k_rope || !v || !out || !lse)
+    return fail(MLA_ERR_INVALID_ARG, "mla_prefill: null tensor pointer");
+  if (B <= 0 || H <= 0 || S <= 0)
+    return fail(MLA_ERR_INVALID_ARG, "mla_prefill: B, H, S must be positive (got %d, %d, %d)", B, H, S);
+  if (B > 65535 || H > 65535)
+    return fail(MLA_ERR_UNSUPPORTED, "mla_prefill: B and H must be at most 65535");
+  if (d_nope != 128 || d_rope != 64 || d_v != 128)
+    return fail(MLA_ERR_UNSUPPORTED, "mla_prefill: only d_nope=128, d_rope=64, d_v=128 are built (got %d, %d, %d)",
+                d_nope, d_rope, d_v);
+  if (!std::isfinite(softmax_scale) || softmax_scale <= 0.f)
+    return fail(MLA_ERR_INVALID_ARG, "mla_prefill: softmax_scale must be finite and positive");
+  const bool fp8 = qkv_dtype == MLA_FP8_E4M3;
+  if (qkv_dtype != MLA_BF16 && !fp8)
+    return fail(MLA_ERR_UNSUPPORTED, "mla_prefill: qkv_dtype must be MLA_BF16 or MLA_FP8_E4M3");
+  if (out_dtype != MLA_BF16 && out_dtype != MLA_FP32)
+    return fail(MLA_ERR_UNSUPPORTED, "mla_prefill: out_dtype must be MLA_BF16 or MLA_FP32");
+  if (fp8 && (!q_scale || !k_scale))
+    return fail(MLA_ERR_INVALID_ARG, "mla_prefill: fp8 inputs need q_scale and k_scale");
+  if (!fp8 && (q_scale || k_scale))
+    return fail(MLA_ERR_INVALID_ARG, "mla_prefill: q_scale/k_scale must be NULL for bf16 inputs");
+  const void* ptrs[] = {q_nope, q_rope, k_nope, k_rope, v, out, lse};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return fail(MLA_ERR_INVALID_ARG, "mla_prefill: tensors must be 16-byte aligned");
+  if ((double)B * S * H * 128 >= 9.0e18)
+    return fail(MLA_ERR_UNSUPPORTED, "mla_prefill: problem too large");
+  unsigned int* err = device_error_word();
+  if (!err) return fail(MLA_ERR_CUDA, "mla_prefill: device error word not reachable");
+  cudaError_t e;
+  if (!fp8)
+    e = mla::launch_prefill_sm103_bf16(q_nope, q_rope, k_nope, k_rope, v, out, lse, B, H, S,
+                                       softmax_scale, causal != 0, out_dtype == MLA_FP32, err,
+                                       static_cast<cudaStream_t>(stream));
+  else
+    e = mla::launch_prefill_simt(q_nope, q_rope, k_nope, k_rope, v, q_scale, k_scale, out, lse,
+                                 B, H, S, softmax_scale, causal != 0, fp8,
+                                 out_dtype == MLA_FP32, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mla_prefill launch");
+  return MLA_OK;
+}
+
+size_t mla_decode_workspace_size(int B, int H, int q_len, int d_latent) {
+  if (B <= 0 || H <= 0 || q_len <= 0 || d_latent <= 0) return 0;
+  const int G = num_sms_current() * kDecodeCtasPerSm;
+  if (G <= 0) return 0;
+  return decode_workspace_layout(nullptr, B, H * q_len, d_latent, G).bytes;
+}
+
+mla_status mla_decode(const void* q_latent, const void* q_rope, const void* kv_cache,
+                      const float* kv_scale, const int* page_table, const int* cache_lens,
+                      void* out, float* lse, int B, int H, int q_len, int d_latent,
+                      int d_rope, int page_size, int max_pages_per_seq, int num_pages,
+                      float softmax_scale, int causal, mla_dtype kv_dtype, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  if (!q_latent || !q_rope || !kv_cache || !page_table || !cache_lens || !out || !lse)
+    return fail(MLA_ERR_INVALID_ARG, "mla_decode: null tensor pointer");
+  if (B <= 0 || H <= 0 || q_len <= 0 || max_pages_per_seq <= 0 || num_pages <= 0)
+    return fail(MLA_ERR_INVALID_ARG, "mla_decode: B, H, q_len, max_pages_per_seq, num_pages must be positive");
+  if (d_latent != 512 || d_rope != 64)
+    return fail(MLA_ERR_UNSUPPORTED, "mla_decode: only d_latent=512, d_rope=64 are built (got %d, %d)", d_latent, d_rope);
+  if (page_size != 64)
+    return fail(MLA_ERR_UNSUPPORTED, "mla_decode: only page_size=64 is built (got %d)", page_size);
+  if (H * q_len > 128)
+    return fail(MLA_ERR_UNSUPPORTED, "mla_decode: q_len*H must be at most 128 (got %d)", H * q_len);
+  if (B > 65535) return fail(MLA_ERR_UNSUPPORTED, "mla_decode: B must be at most 65535");
+  if ((long long)max_pages_per_seq * page_size > 0x7fffffffLL)
+    return fail(MLA_ERR_UNSUPPORTED, "mla_decode: max_pages_per_seq*page_size overflows int32");
+  if (!std::isfinite(softmax_scale) || softmax_scale <= 0.f)
+    return fail(MLA_ERR_INVALID_ARG, "mla_decode: softmax_scale must be finite and positive");
+  const bool fp8 = kv_dtype == MLA_FP8_E4M3;
+  if (kv_dtype != MLA_BF16 && !fp8)
+    return fail(MLA_ERR_UNSUPPORTED, "mla_decode: kv_dtype must be MLA_BF16 or MLA_FP8_E4M3");
+  if (fp8 != (kv_scale != nullptr))
+    return fail(MLA_ERR_INVALID_ARG, "mla_decode: kv_scale is required for fp8 and must be NULL for bf16");
+  const void* ptrs[] = {q_latent, q_rope, kv_cache, out, lse, workspace};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return fail(MLA_ERR_INVALID_ARG, "mla_decode: tensors must be 16-byte aligned");
+  const int G = num_sms_current() * kDecodeCtasPerSm;
+  if (G <= 0) return fail(MLA_ERR_CUDA, "mla_decode: cannot query the SM count");
+  DecodeWorkspace ws = decode_workspace_layout(workspace, B, H * q_len, d_latent, G);
+  if (!workspace || workspace_bytes < ws.bytes)
+    return fail(MLA_ERR_WORKSPACE, "mla_decode: workspace of %zu bytes is smaller than the %zu needed",
+                workspace_bytes, ws.bytes);
+  unsigned int* err = device_error_word();
+  if (!err) return fail(MLA_ERR_CUDA, "mla_decode: device error word not reachable");
+  cudaError_t e = mla::launch_decode_simt(q_latent, q_rope, kv_cache, kv_scale, page_table,
+                                          cache_lens, out, lse, B, H, q_len, max_pages_per_seq,
+                                          num_pages, softmax_scale, causal != 0, fp8, ws.part_o,
+                                          ws.part_lse, G, err, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mla_decode launch");
+  return MLA_OK;
+}
+
+}  // extern "C"

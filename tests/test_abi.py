@@ -1,0 +1,97 @@
+"""The C-ABI library: it loads, exports every declared entry point, and rejects bad
+arguments on the host before any launch (CPU only: no call here reaches a kernel)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def clib():
+    lib_path = os.path.join(ROOT, "mla_flash_attention_gb300", "libmla_gb300.so")
+    if not os.path.exists(lib_path):
+        from mla_flash_attention_gb300 import build
+
+        build.build()
+    return ctypes.CDLL(lib_path)
+
+
+def declared_functions():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", h)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(mla_\w+)\s*\(", src, re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("mla_prefill", "mla_decode", "mla_decode_workspace_size", "mla_check_device_error",
+              "mla_last_error", "mla_version"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(clib):
+    for n in declared_functions():
+        assert hasattr(clib, n), n
+
+
+def _prefill(clib, **kw):
+    a = dict(q_nope=16, q_rope=16, k_nope=16, k_rope=16, v=16, q_scale=None, k_scale=None,
+             out=16, lse=16, B=1, H=1, S=1, dn=128, dr=64, dv=128, scale=0.1, causal=1, dt=0,
+             odt=0)
+    a.update(kw)
+    f = clib.mla_prefill
+    f.restype = ctypes.c_int
+    P = ctypes.c_void_p
+    return f(P(a["q_nope"]), P(a["q_rope"]), P(a["k_nope"]), P(a["k_rope"]), P(a["v"]),
+             P(a["q_scale"]), P(a["k_scale"]), P(a["out"]), P(a["lse"]), a["B"], a["H"], a["S"],
+             a["dn"], a["dr"], a["dv"], ctypes.c_float(a["scale"]), a["causal"], a["dt"],
+             a["odt"], None)
+
+
+def test_prefill_argument_checks(clib):
+    # every case below is rejected before any CUDA call (pointers are never dereferenced)
+    assert _prefill(clib, q_nope=None) == 1
+    assert _prefill(clib, S=0) == 1
+    assert _prefill(clib, B=-1) == 1
+    assert _prefill(clib, dn=64) == 2
+    assert _prefill(clib, dv=512) == 2
+    assert _prefill(clib, dt=7) == 2
+    assert _prefill(clib, odt=1) == 2
+    assert _prefill(clib, dt=1) == 1           # fp8 without scales
+    assert _prefill(clib, q_scale=16) == 1     # bf16 with scales
+    assert _prefill(clib, q_rope=24) == 1      # misaligned
+    assert _prefill(clib, scale=float("nan")) == 1
+    clib.mla_last_error.restype = ctypes.c_char_p
+    assert b"softmax_scale" in clib.mla_last_error()
+
+
+def _decode(clib, **kw):
+    a = dict(ql=16, qr=16, cache=16, ks=None, pt=16, lens=16, out=16, lse=16, B=1, H=16, T=1,
+             dl=512, dr=64, ps=64, mp=1, npages=1, scale=0.1, causal=1, dt=0, ws=None, wsb=0)
+    a.update(kw)
+    f = clib.mla_decode
+    f.restype = ctypes.c_int
+    P = ctypes.c_void_p
+    return f(P(a["ql"]), P(a["qr"]), P(a["cache"]), P(a["ks"]), P(a["pt"]), P(a["lens"]),
+             P(a["out"]), P(a["lse"]), a["B"], a["H"], a["T"], a["dl"], a["dr"], a["ps"], a["mp"],
+             a["npages"], ctypes.c_float(a["scale"]), a["causal"], a["dt"], P(a["ws"]),
+             ctypes.c_size_t(a["wsb"]), None)
+
+
+def test_decode_argument_checks(clib):
+    assert _decode(clib, ql=None) == 1
+    assert _decode(clib, B=0) == 1
+    assert _decode(clib, dl=256) == 2
+    assert _decode(clib, ps=32) == 2
+    assert _decode(clib, H=128, T=2) == 2      # more than 128 query rows
+    assert _decode(clib, dt=1) == 1            # fp8 without scales
+    assert _decode(clib, ks=16) == 1           # bf16 with scales
+    assert _decode(clib, out=8) == 1           # misaligned
+    assert _decode(clib, npages=0) == 1
