@@ -1,0 +1,500 @@
+// Absorbed MLA decode over the paged latent cache on tcgen05 / TMEM (split-KV part).
+//
+// Each work unit (a contiguous range of pages from the split plan) is served by a pair
+// of CTAs that differ only in which half of the 512 latent output columns they own:
+// O (128 query rows x 512 fp32) is exactly the 512-column TMEM, so one CTA cannot also
+// hold the scores.  Both CTAs of a pair compute the full scores S = Q C' (the redundant
+// part) and their own half of O += P C[:, half].  Query rows are the (token, head) pairs
+// of one sequence, padded to the MMA's M = 128.
+//
+// Per CTA (12 warps):
+//   warp 0      TMA producer of cache pages (bf16 cache): 64 keys x 576 columns per stage
+//   warp 1      MMA issuer: S(g) = Q C(g)' into one of two S buffers (A operand = Q:
+//               latent 0..255 from TMEM, latent 256..511 + rope from shared memory),
+//               then O_half += P(g) C(g)[:, half] with P read from TMEM
+//   warps 2-3   stage preparation: zero the rows past the sequence end of a partial page
+//               (bf16), or load + convert an fp8 page to bf16 and stage its row scales
+//   warps 4-7   softmax, one thread per query row; they also load each sequence's Q and
+//               write the split's partial (O_half / l, log-sum-exp)
+// TMEM columns: [0,128) Q latent 0..255 (bf16 pairs), [128,256) two S / P buffers of 64,
+// [256,512) O half.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "sm103_ptx.cuh"
+
+namespace mla {
+namespace sm103_decode {
+
+constexpr int kPage = 64, kDl = 512, kDc = 576, kRows = 128;
+constexpr int kPageChunk = kPage * 128;       // 64 rows x 64 bf16 (8 KB), 128B-swizzled
+constexpr int kStageBytes = 9 * kPageChunk;   // 72 KB
+constexpr int kStages = 2;
+constexpr int kQChunk = kRows * 128;          // 128 rows x 64 bf16 (16 KB)
+constexpr int kOffQhi = 0;                    // latent 256..511 (4 chunks) + rope (1 chunk)
+constexpr int kOffStage = 5 * kQChunk;        // 80 KB
+constexpr int kSmemBytes = kOffStage + kStages * kStageBytes;  // 224 KB
+constexpr int kSmemAlloc = kSmemBytes + 1024;
+constexpr int kThreads = 384;
+constexpr int kPrepThreads = 64;
+
+struct Params {
+  const uint16_t* q_latent;  // [B, T, H, 512]
+  const uint16_t* q_rope;    // [B, T, H, 64]
+  const uint8_t* cache8;     // fp8 cache [num_pages, 64, 576] (fp8 path)
+  const float* kv_scale;     // [num_pages, 64] (fp8 path)
+  const int* page_table;
+  const int* cache_lens;
+  float* part_o;
+  float* part_lse;
+  unsigned int* err;
+  int B, H, T, max_pages, num_pages, causal, G;
+  float scale_log2;
+};
+
+struct Bars {
+  uint64_t stage_full[kStages], stage_ready[kStages], stage_empty[kStages];
+  uint64_t s_full[2], p_full[2], o_done, q_ready;
+  uint32_t tmem_base;
+  int abort_flag;
+  float kscale[kStages][kPage];
+};
+
+__device__ __forceinline__ int clamp_len(int L, int max_pages) {
+  return min(max(L, 0), max_pages * kPage);
+}
+
+// Walks the (sequence, page range) segments of this CTA's work unit in order; every
+// role runs its own copy and sees the same sequence.
+struct Segments {
+  const Params* p;
+  int start, end;  // flat page range
+  int b, pb;       // current sequence and its first flat page
+  __device__ void init(const Params& prm, int unit) {
+    p = &prm;
+    int total = 0;
+    for (int i = 0; i < prm.B; ++i) total += pages_of(clamp_len(__ldg(prm.cache_lens + i), prm.max_pages), kPage);
+    const int chunk = total > 0 ? (total + prm.G - 1) / prm.G : 1;
+    start = unit * chunk;
+    end = min(total, start + chunk);
+    b = 0;
+    pb = 0;
+  }
+  // Next non-empty segment: sets seq, L, lo, hi (page indices within the sequence).
+  __device__ bool next(int& seq, int& L, int& lo, int& hi) {
+    while (b < p->B && pb < end) {
+      const int Lb = clamp_len(__ldg(p->cache_lens + b), p->max_pages);
+      const int n = pages_of(Lb, kPage);
+      const int l0 = max(start, pb) - pb, h0 = min(end, pb + n) - pb;
+      const int cur = b;
+      pb += n;
+      ++b;
+      if (l0 < h0) {
+        seq = cur;
+        L = Lb;
+        lo = l0;
+        hi = h0;
+        return true;
+      }
+    }
+    return false;
+  }
+};
+
+template <bool kFp8>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_split_kernel(const __grid_constant__ CUtensorMap tm_cache, const Params p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  __shared__ Bars bars;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int unit = blockIdx.x >> 1, half = blockIdx.x & 1;
+  const int TH = p.T * p.H;
+
+  if (threadIdx.x == 0) {
+    bars.abort_flag = 0;
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(&bars.stage_full[s], 1);
+      ptx::mbar_init(&bars.stage_ready[s], kPrepThreads);
+      ptx::mbar_init(&bars.stage_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&bars.s_full[i], 1);
+      ptx::mbar_init(&bars.p_full[i], kRows);
+    }
+    ptx::mbar_init(&bars.o_done, 1);
+    ptx::mbar_init(&bars.q_ready, kRows);
+    ptx::fence_barrier_init();
+  }
+  if (warp == 2) ptx::tmem_alloc(&bars.tmem_base, 512);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+  volatile int* abort_flag = &bars.abort_flag;
+  Segments segs;
+  segs.init(p, unit);
+  int seq, L, lo, hi;
+
+  if (warp < 4) {
+    ptx::regs_dec<56>();
+    if (warp == 0) {
+      // ------------------------------------------------------------ TMA producer (bf16)
+      if (!kFp8 && ptx::elect_one()) {
+        int g = 0;
+        bool ok = true;
+        while (ok && segs.next(seq, L, lo, hi)) {
+          for (int pg = lo; pg < hi; ++pg, ++g) {
+            const int s = g % kStages;
+            if (!(ok = ptx::mbar_wait(&bars.stage_empty[s], ((g / kStages) & 1) ^ 1, abort_flag, p.err))) break;
+            const int page = __ldg(p.page_table + (size_t)seq * p.max_pages + pg);
+            // an out-of-range page reads as zeros (outside the tensor) and is masked later
+            const int y = (page >= 0 && page < p.num_pages) ? page * kPage : -2 * kPage;
+            unsigned char* dst = sm + kOffStage + s * kStageBytes;
+            ptx::mbar_arrive_expect_tx(&bars.stage_full[s], kStageBytes);
+#pragma unroll 1
+            for (int c = 0; c < 9; ++c)
+              ptx::tma_load_2d(dst + c * kPageChunk, &tm_cache, &bars.stage_full[s], c * 64, y);
+            // warm L2 with the page two steps ahead of this one (same sequence only)
+            if (half == 0 && pg + 2 < hi) {
+              const int ahead = __ldg(p.page_table + (size_t)seq * p.max_pages + pg + 2);
+              if (ahead >= 0 && ahead < p.num_pages)
+#pragma unroll 1
+                for (int c = 0; c < 9; ++c) ptx::tma_prefetch_2d(&tm_cache, c * 64, ahead * kPage);
+            }
+          }
+        }
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer
+      if (ptx::elect_one()) {
+        constexpr uint32_t kIdS = ptx::make_idesc(1, kRows, kPage, 0, 0);
+        constexpr uint32_t kIdPV = ptx::make_idesc(1, kRows, 256, 0, 1);
+        const uint32_t qhi = ptx::smem_u32(sm + kOffQhi);
+        const uint32_t stage0 = ptx::smem_u32(sm + kOffStage);
+        const uint32_t o_tm = tmem + 256;
+        int g = 0, nseg = 0;
+        bool ok = true;
+        auto issue_s = [&](int gg) {
+          const uint32_t st = stage0 + (gg % kStages) * kStageBytes;
+          const uint32_t d = tmem + 128 + (gg & 1) * 64;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {  // latent 0..255: A from TMEM
+            const uint64_t db = ptx::sw128_desc(st + (k >> 2) * kPageChunk + (k & 3) * 32, 16, 1024);
+            ptx::mma_bf16_ts(d, tmem + k * 8, db, kIdS, k > 0);
+          }
+#pragma unroll
+          for (int k = 16; k < 36; ++k) {  // latent 256..511 + rope: A from shared memory
+            const int kq = k - 16;
+            const uint64_t da = ptx::sw128_desc(qhi + (kq >> 2) * kQChunk + (kq & 3) * 32, 16, 1024);
+            const uint64_t db = ptx::sw128_desc(st + (k >> 2) * kPageChunk + (k & 3) * 32, 16, 1024);
+            ptx::mma_bf16_ss(d, da, db, kIdS, 1);
+          }
+        };
+        while (ok && segs.next(seq, L, lo, hi)) {
+          // Q of this sequence (TMEM + shared memory) is written by the softmax warps
+          if (!(ok = ptx::mbar_wait(&bars.q_ready, nseg & 1, abort_flag, p.err))) break;
+          ptx::tc_fence_after();
+          const int n = hi - lo, g0 = g;
+          if (!(ok = ptx::mbar_wait(&bars.stage_ready[g0 % kStages], (g0 / kStages) & 1, abort_flag, p.err))) break;
+          ptx::tc_fence_after();
+          issue_s(g0);
+          ptx::mma_commit(&bars.s_full[g0 & 1]);
+          for (int i = 0; i < n; ++i, ++g) {
+            if (i + 1 < n) {
+              const int g1 = g + 1;
+              if (!(ok = ptx::mbar_wait(&bars.stage_ready[g1 % kStages], (g1 / kStages) & 1, abort_flag, p.err))) break;
+              ptx::tc_fence_after();
+              issue_s(g1);
+              ptx::mma_commit(&bars.s_full[g1 & 1]);
+            }
+            if (!(ok = ptx::mbar_wait(&bars.p_full[g & 1], (g >> 1) & 1, abort_flag, p.err))) break;
+            ptx::tc_fence_after();
+            const uint32_t st = stage0 + (g % kStages) * kStageBytes + 4 * half * kPageChunk;
+            const uint32_t pa = tmem + 128 + (g & 1) * 64;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t db = ptx::sw128_desc(st + k * 2048, kPageChunk, 1024);
+              ptx::mma_bf16_ts(o_tm, pa + k * 8, db, kIdPV, (i > 0 || k > 0) ? 1u : 0u);
+            }
+            ptx::mma_commit(&bars.o_done);
+            ptx::mma_commit(&bars.stage_empty[g % kStages]);
+          }
+          ++nseg;
+        }
+      }
+    } else {
+      // ------------------------------------------------------------ stage preparation
+      const int tid = threadIdx.x - 64;  // 0..63
+      int g = 0;
+      bool ok = true;
+      while (ok && segs.next(seq, L, lo, hi)) {
+        for (int pg = lo; pg < hi; ++pg, ++g) {
+          const int s = g % kStages;
+          unsigned char* st = sm + kOffStage + s * kStageBytes;
+          const int valid = min(kPage, L - pg * kPage);  // rows holding tokens of this sequence
+          const int page = __ldg(p.page_table + (size_t)seq * p.max_pages + pg);
+          const bool bad = page < 0 || page >= p.num_pages;
+          if (bad && tid == 0) latch_error(p.err, kErrBadPage);
+          if constexpr (!kFp8) {
+            ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.stage_full[s], (g / kStages) & 1, abort_flag, p.err));
+            if (!ok) break;
+            if (valid < kPage) {
+              // zero rows valid..63 of all 9 chunks (16-byte granules)
+              const int nrow = kPage - valid;
+              for (int e = tid; e < nrow * 9 * 8; e += kPrepThreads) {
+                const int row = valid + e / 72, rem = e % 72, c = rem >> 3, gr = rem & 7;
+                *reinterpret_cast<uint4*>(st + c * kPageChunk + row * 128 + gr * 16) = make_uint4(0, 0, 0, 0);
+              }
+            }
+          } else {
+            ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.stage_empty[s], ((g / kStages) & 1) ^ 1, abort_flag, p.err));
+            if (!ok) break;
+            // 64 rows x 576 fp8 -> bf16, row-swizzled chunks; one thread per row
+            const int row = tid;
+            const bool live = !bad && row < valid;
+            const uint8_t* src = p.cache8 + ((size_t)(bad ? 0 : page) * kPage + row) * kDc;
+            bars.kscale[s][row] = live ? __ldg(p.kv_scale + (size_t)page * kPage + row) : 0.f;
+#pragma unroll 1
+            for (int c = 0; c < 9; ++c) {
+              uint4 raw[4];
+#pragma unroll
+              for (int x = 0; x < 4; ++x)
+                raw[x] = live ? __ldg(reinterpret_cast<const uint4*>(src + c * 64) + x) : make_uint4(0, 0, 0, 0);
+              const uint8_t* bytes = reinterpret_cast<const uint8_t*>(raw);
+              unsigned char* dst = st + c * kPageChunk + row * 128;
+#pragma unroll
+              for (int gr = 0; gr < 8; ++gr) {
+                uint32_t w[4];
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                  const float a = e4m3_to_f32(bytes[gr * 8 + 2 * x]);
+                  const float bq = e4m3_to_f32(bytes[gr * 8 + 2 * x + 1]);
+                  w[x] = ptx::pack_bf16x2(a, bq);
+                }
+                *reinterpret_cast<uint4*>(dst + ((gr ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+              }
+            }
+          }
+          ptx::fence_proxy_async();
+          ptx::mbar_arrive(&bars.stage_ready[s]);
+        }
+      }
+    }
+  } else {
+    // -------------------------------------------------------------- softmax / Q / epilogue
+    ptx::regs_inc<224>();
+    const int r = threadIdx.x - 128;  // query row == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int t_row = r / p.H;
+    int g = 0, nseg = 0;
+    bool ok = true;
+    while (ok && segs.next(seq, L, lo, hi)) {
+      // the previous segment's MMAs are done (its epilogue waited for the last PV), so
+      // Q can be overwritten: latent 0..255 -> TMEM columns 0..127, the rest -> smem
+      {
+        const bool live = r < TH;
+        const size_t qrow = (size_t)seq * TH + r;
+        const uint4* ql = reinterpret_cast<const uint4*>(p.q_latent + qrow * kDl);
+        const uint4* qr = reinterpret_cast<const uint4*>(p.q_rope + qrow * 64);
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {  // 4 x 32 TMEM columns = 4 x 64 bf16
+          uint32_t v[32];
+#pragma unroll
+          for (int x = 0; x < 8; ++x) {
+            const uint4 u = live ? __ldg(ql + c * 8 + x) : make_uint4(0, 0, 0, 0);
+            v[4 * x] = u.x; v[4 * x + 1] = u.y; v[4 * x + 2] = u.z; v[4 * x + 3] = u.w;
+          }
+          ptx::tmem_st32(tmem + lane_off + c * 32, v);
+        }
+#pragma unroll 1
+        for (int c = 0; c < 5; ++c) {  // latent 256..511 (4 chunks) + rope (1 chunk)
+          unsigned char* dst = sm + kOffQhi + c * kQChunk + r * 128;
+#pragma unroll
+          for (int x = 0; x < 8; ++x) {
+            const uint4 u = !live ? make_uint4(0, 0, 0, 0) : (c < 4 ? __ldg(ql + 32 + c * 8 + x) : __ldg(qr + x));
+            *reinterpret_cast<uint4*>(dst + ((x ^ (r & 7)) << 4)) = u;
+          }
+        }
+        ptx::tmem_st_wait();
+        ptx::fence_proxy_async();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&bars.q_ready);
+      }
+      const int last_visible = p.causal ? (L - p.T + t_row) : (L - 1);  // keys <= this are visible
+      float m = -INFINITY, l = 0.f;
+      const uint32_t o_addr = tmem + lane_off + 256;
+      for (int pg = lo; pg < hi; ++pg, ++g) {
+        ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.s_full[g & 1], (g >> 1) & 1, abort_flag, p.err));
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const uint32_t s_addr = tmem + lane_off + 128 + (g & 1) * 64;
+        float s[64];
+        {
+          uint32_t v[32];
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            ptx::tmem_ld32(s_addr + c * 32, v);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int x = 0; x < 32; ++x) s[c * 32 + x] = __uint_as_float(v[x]);
+          }
+        }
+        const int page = __ldg(p.page_table + (size_t)seq * p.max_pages + pg);
+        const bool bad = page < 0 || page >= p.num_pages;
+        const int key0 = pg * kPage;
+        const int lim = bad ? -1 : min(last_visible, L - 1);  // visible keys: key0+x <= lim
+        float mx = -INFINITY;
+#pragma unroll
+        for (int x = 0; x < 64; ++x) {
+          float v = s[x];
+          if constexpr (kFp8) v *= bars.kscale[g % kStages][x];
+          v = (key0 + x <= lim) ? v * p.scale_log2 : -INFINITY;
+          s[x] = v;
+          mx = fmaxf(mx, v);
+        }
+        float m_use = m;
+        if (pg == lo) {
+          m_use = mx;
+        } else {
+          const bool grow = mx > m + 8.0f;
+          if (__any_sync(0xffffffffu, grow)) {
+            ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.o_done, (g - 1) & 1, abort_flag, p.err));
+            if (!ok) break;
+            ptx::tc_fence_after();
+            const float alpha = grow ? ptx::ex2(m - mx) : 1.f;  // m = -inf gives 0
+            if (grow) m_use = mx;
+            uint32_t v[32];
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {
+              ptx::tmem_ld32(o_addr + c * 32, v);
+              ptx::tmem_ld_wait();
+#pragma unroll
+              for (int x = 0; x < 32; ++x) v[x] = __float_as_uint(__uint_as_float(v[x]) * alpha);
+              ptx::tmem_st32(o_addr + c * 32, v);
+            }
+            l *= alpha;
+          }
+        }
+        m = m_use;
+        const float neg_m = (m == -INFINITY) ? 0.f : -m;
+        float psum = 0.f;
+        uint32_t pk[32];
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+          const float p0 = ptx::ex2(s[2 * x] + neg_m);
+          const float p1 = ptx::ex2(s[2 * x + 1] + neg_m);
+          if constexpr (kFp8) {
+            psum += p0 + p1;
+            pk[x] = ptx::pack_bf16x2(p0 * bars.kscale[g % kStages][2 * x],
+                                     p1 * bars.kscale[g % kStages][2 * x + 1]);
+          } else {
+            // sum the bf16-rounded values the PV product uses (exact for a dominant key)
+            const uint32_t w = ptx::pack_bf16x2(p0, p1);
+            pk[x] = w;
+            psum += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+          }
+        }
+        l += psum;
+        ptx::tmem_st32(s_addr, pk);
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&bars.p_full[g & 1]);
+      }
+      if (!ok) break;
+      // epilogue of the segment: partial (O_half / l, LSE) into slot unit + seq
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.o_done, (g - 1) & 1, abort_flag, p.err));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const size_t slot = (size_t)unit + seq;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      float* dst = p.part_o + (slot * TH + r) * kDl + half * 256;
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        uint32_t v[32];
+        ptx::tmem_ld32(o_addr + c * 32, v);
+        ptx::tmem_ld_wait();
+        if (r < TH) {
+#pragma unroll
+          for (int x = 0; x < 8; ++x)
+            reinterpret_cast<float4*>(dst + c * 32)[x] =
+                make_float4(__uint_as_float(v[4 * x]) * inv, __uint_as_float(v[4 * x + 1]) * inv,
+                            __uint_as_float(v[4 * x + 2]) * inv, __uint_as_float(v[4 * x + 3]) * inv);
+        }
+      }
+      if (half == 0 && r < TH)
+        p.part_lse[slot * TH + r] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+      ptx::tc_fence_before();
+      ++nseg;
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace sm103_decode
+
+// ---------------------------------------------------------------- host side
+
+cudaError_t encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* ptr,
+                              const uint64_t* dims, const uint64_t* strides, const uint32_t* box);
+
+cudaError_t launch_decode_sm103(const void* q_latent, const void* q_rope, const void* kv_cache,
+                                const float* kv_scale, const int* page_table,
+                                const int* cache_lens, int B, int H, int T, int max_pages,
+                                int num_pages, float softmax_scale, int causal, bool fp8,
+                                float* part_o, float* part_lse, int G, unsigned int* err,
+                                cudaStream_t stream) {
+  using namespace sm103_decode;
+  CUtensorMap tm;
+  memset(&tm, 0, sizeof(tm));
+  if (!fp8) {
+    uint64_t dims[2] = {(uint64_t)kDc, (uint64_t)num_pages * kPage};
+    uint64_t strides[1] = {(uint64_t)kDc * 2};
+    uint32_t box[2] = {64, kPage};
+    cudaError_t e = encode_tensor_map(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_cache, dims,
+                                      strides, box);
+    if (e != cudaSuccess) return e;
+  }
+  Params p;
+  p.q_latent = static_cast<const uint16_t*>(q_latent);
+  p.q_rope = static_cast<const uint16_t*>(q_rope);
+  p.cache8 = static_cast<const uint8_t*>(kv_cache);
+  p.kv_scale = kv_scale;
+  p.page_table = page_table;
+  p.cache_lens = cache_lens;
+  p.part_o = part_o;
+  p.part_lse = part_lse;
+  p.err = err;
+  p.B = B;
+  p.H = H;
+  p.T = T;
+  p.max_pages = max_pages;
+  p.num_pages = num_pages;
+  p.causal = causal;
+  p.G = G;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  auto go = [&](auto kern) -> cudaError_t {
+    static bool checked[2] = {false, false};
+    if (!checked[fp8 ? 1 : 0]) {
+      cudaFuncAttributes fa;
+      cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+      if (e != cudaSuccess) return e;
+      if (fa.numRegs != 168) return cudaErrorInvalidDeviceFunction;  // setmaxnreg split
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+      if (e != cudaSuccess) return e;
+      checked[fp8 ? 1 : 0] = true;
+    }
+    kern<<<2 * G, kThreads, kSmemAlloc, stream>>>(tm, p);
+    return cudaGetLastError();
+  };
+  return fp8 ? go(decode_split_kernel<true>) : go(decode_split_kernel<false>);
+}
+
+}  // namespace mla

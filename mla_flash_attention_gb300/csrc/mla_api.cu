@@ -21,12 +21,20 @@ cudaError_t launch_prefill_sm103_bf16(const void* q_nope, const void* q_rope, co
                                       const void* k_rope, const void* v, void* out, float* lse,
                                       int B, int H, int S, float softmax_scale, int causal,
                                       bool out_f32, unsigned int* err, cudaStream_t stream);
-cudaError_t launch_decode_simt(const void* q_latent, const void* q_rope, const void* kv_cache,
-                               const float* kv_scale, const int* page_table,
-                               const int* cache_lens, void* out, float* lse, int B, int H,
-                               int T, int max_pages, int num_pages, float softmax_scale,
-                               int causal, bool fp8, float* part_o, float* part_lse, int G,
-                               unsigned int* err, cudaStream_t stream);
+cudaError_t launch_prefill_sm103_fp8(const void* q_nope, const void* q_rope, const void* k_nope,
+                                     const void* k_rope, const void* v, const float* q_scale,
+                                     const float* k_scale, void* out, float* lse, int B, int H,
+                                     int S, float softmax_scale, int causal, bool out_f32,
+                                     unsigned int* err, cudaStream_t stream);
+cudaError_t launch_decode_sm103(const void* q_latent, const void* q_rope, const void* kv_cache,
+                                const float* kv_scale, const int* page_table,
+                                const int* cache_lens, int B, int H, int T, int max_pages,
+                                int num_pages, float softmax_scale, int causal, bool fp8,
+                                float* part_o, float* part_lse, int G, unsigned int* err,
+                                cudaStream_t stream);
+cudaError_t launch_decode_combine(const float* part_o, const float* part_lse,
+                                  const int* cache_lens, void* out, float* lse, int B, int H,
+                                  int T, int max_pages, int G, cudaStream_t stream);
 }  // namespace mla
 
 namespace {
@@ -71,7 +79,9 @@ int num_sms_current() {
   return n;
 }
 
-constexpr int kDecodeCtasPerSm = 1;
+// Decode work units: each unit is served by a pair of CTAs (one per half of the latent
+// output columns), one CTA per SM.
+int decode_units() { return num_sms_current() / 2; }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -155,16 +165,17 @@ mla_status mla_prefill(const void* q_nope, const void* q_rope, const void* k_nop
                                        softmax_scale, causal != 0, out_dtype == MLA_FP32, err,
                                        static_cast<cudaStream_t>(stream));
   else
-    e = mla::launch_prefill_simt(q_nope, q_rope, k_nope, k_rope, v, q_scale, k_scale, out, lse,
-                                 B, H, S, softmax_scale, causal != 0, fp8,
-                                 out_dtype == MLA_FP32, static_cast<cudaStream_t>(stream));
+    e = mla::launch_prefill_sm103_fp8(q_nope, q_rope, k_nope, k_rope, v, q_scale, k_scale, out,
+                                      lse, B, H, S, softmax_scale, causal != 0,
+                                      out_dtype == MLA_FP32, err,
+                                      static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "mla_prefill launch");
   return MLA_OK;
 }
 
 size_t mla_decode_workspace_size(int B, int H, int q_len, int d_latent) {
   if (B <= 0 || H <= 0 || q_len <= 0 || d_latent <= 0) return 0;
-  const int G = num_sms_current() * kDecodeCtasPerSm;
+  const int G = decode_units();
   if (G <= 0) return 0;
   return decode_workspace_layout(nullptr, B, H * q_len, d_latent, G).bytes;
 }
@@ -198,7 +209,7 @@ mla_status mla_decode(const void* q_latent, const void* q_rope, const void* kv_c
   const void* ptrs[] = {q_latent, q_rope, kv_cache, out, lse, workspace};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return fail(MLA_ERR_INVALID_ARG, "mla_decode: tensors must be 16-byte aligned");
-  const int G = num_sms_current() * kDecodeCtasPerSm;
+  const int G = decode_units();
   if (G <= 0) return fail(MLA_ERR_CUDA, "mla_decode: cannot query the SM count");
   DecodeWorkspace ws = decode_workspace_layout(workspace, B, H * q_len, d_latent, G);
   if (!workspace || workspace_bytes < ws.bytes)
@@ -206,10 +217,14 @@ mla_status mla_decode(const void* q_latent, const void* q_rope, const void* kv_c
                 workspace_bytes, ws.bytes);
   unsigned int* err = device_error_word();
   if (!err) return fail(MLA_ERR_CUDA, "mla_decode: device error word not reachable");
-  cudaError_t e = mla::launch_decode_simt(q_latent, q_rope, kv_cache, kv_scale, page_table,
-                                          cache_lens, out, lse, B, H, q_len, max_pages_per_seq,
-                                          num_pages, softmax_scale, causal != 0, fp8, ws.part_o,
-                                          ws.part_lse, G, err, static_cast<cudaStream_t>(stream));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = mla::launch_decode_sm103(q_latent, q_rope, kv_cache, kv_scale, page_table,
+                                           cache_lens, B, H, q_len, max_pages_per_seq, num_pages,
+                                           softmax_scale, causal != 0, fp8, ws.part_o,
+                                           ws.part_lse, G, err, st);
+  if (e == cudaSuccess)
+    e = mla::launch_decode_combine(ws.part_o, ws.part_lse, cache_lens, out, lse, B, H, q_len,
+                                   max_pages_per_seq, G, st);
   if (e != cudaSuccess) return cuda_fail(e, "mla_decode launch");
   return MLA_OK;
 }

@@ -1,0 +1,475 @@
+// Fused MLA prefill with fp8 e4m3 Q_nope / K_nope / V and one fp32 scale per query and per
+// key token (tcgen05 + TMEM + TMA).
+//
+// Score: s_ij = scale * (qs_i ks_j (Qn8_i . Kn8_j) + Qr_i . Kr_j).  The per-token scales are
+// folded so that one fp32 accumulator serves both depths:
+//   acc_ij = Qn8_i . Kn8_j + (Qr_i / qs_i) . (Kr_j / ks_j),   s_ij = scale qs_i ks_j acc_ij,
+// with the nope product on the 8-bit MMA (kind::f8f6f4) and the rescaled rope product on the
+// bf16 MMA.  V_j = ks_j V8_j, so the PV product uses P'_ij = p_ij ks_j against V8 widened to
+// bf16 (exact); P' is split into a bf16 high part and a bf16 low part (two MMAs) so the
+// product keeps ~16 significant bits -- O reaches |O| ~ 40 on the fp8 workload and is
+// accumulated and written in fp32.
+//
+// Roles (12 warps): warp 0 TMA producer; warp 1 MMA issuer; warps 2-3 converters (rope
+// rescaling by 1/scale, V8 -> bf16 into a 128B-swizzled N-major tile, key scales into smem);
+// warps 4-7 / 8-11 softmax of Q tiles 0 / 1 (as in the bf16 kernel).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "sm103_ptx.cuh"
+
+namespace mla {
+namespace sm103_prefill_fp8 {
+
+constexpr int BM = 128, BN = 128, NQ = 2;
+constexpr int kChunk = 128 * 128;          // 128 rows x 128 bytes
+constexpr int kStages = 2;
+constexpr int kOffQn = 0;                                  // NQ x 16 KB (fp8)
+constexpr int kOffQr = kOffQn + NQ * kChunk;               // NQ x 16 KB (bf16 rope / qs)
+constexpr int kOffKn = kOffQr + NQ * kChunk;               // stages x 16 KB
+constexpr int kOffKr = kOffKn + kStages * kChunk;          // stages x 16 KB
+constexpr int kOffV8 = kOffKr + kStages * kChunk;          // stages x 16 KB
+constexpr int kOffVb = kOffV8 + kStages * kChunk;          // stages x 32 KB
+constexpr int kSmemBytes = kOffVb + kStages * 2 * kChunk;  // 224 KB
+constexpr int kSmemAlloc = kSmemBytes + 1024;
+constexpr int kThreads = 384;
+constexpr int kConvThreads = 64;
+
+struct Params {
+  int B, H, S, causal, nrb, out_f32;
+  float scale_log2;
+  const float* q_scale;
+  const float* k_scale;
+  void* out;
+  float* lse;
+  unsigned int* err;
+};
+
+struct Bars {
+  uint64_t q_full, q_conv;
+  uint64_t k_full[kStages], k_conv[kStages], k_empty[kStages];
+  uint64_t v8_full[kStages], v8_empty[kStages], vb_full[kStages], vb_empty[kStages];
+  uint64_t s_full[NQ], p_full[NQ], o_done[NQ];
+  uint32_t tmem_base;
+  int abort_flag;
+  float ks[kStages][BN];
+};
+
+__device__ __forceinline__ int n_kv_tiles(const Params& p, int q_row0) {
+  const int all = (p.S + BN - 1) / BN;
+  return p.causal ? min(all, (q_row0 + NQ * BM + BN - 1) / BN) : all;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_scale(uint32_t w, float f) {
+  const float lo = __uint_as_float(w << 16) * f;
+  const float hi = __uint_as_float(w & 0xffff0000u) * f;
+  return ptx::pack_bf16x2(lo, hi);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_fp8_kernel(const __grid_constant__ CUtensorMap tm_qn,
+                       const __grid_constant__ CUtensorMap tm_qr,
+                       const __grid_constant__ CUtensorMap tm_kn,
+                       const __grid_constant__ CUtensorMap tm_kr,
+                       const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  __shared__ Bars bars;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int bid = blockIdx.x;
+  const int bh = bid / p.nrb;
+  const int rb = p.nrb - 1 - (bid % p.nrb);
+  const int b = bh / p.H, h = bh % p.H;
+  const int q_row0 = rb * NQ * BM;
+  const int n_kv = n_kv_tiles(p, q_row0);
+
+  if (threadIdx.x == 0) {
+    bars.abort_flag = 0;
+    ptx::mbar_init(&bars.q_full, 1);
+    ptx::mbar_init(&bars.q_conv, kConvThreads);
+    for (int i = 0; i < kStages; ++i) {
+      ptx::mbar_init(&bars.k_full[i], 1);
+      ptx::mbar_init(&bars.k_conv[i], kConvThreads);
+      ptx::mbar_init(&bars.k_empty[i], 1);
+      ptx::mbar_init(&bars.v8_full[i], 1);
+      ptx::mbar_init(&bars.v8_empty[i], kConvThreads);
+      ptx::mbar_init(&bars.vb_full[i], kConvThreads);
+      ptx::mbar_init(&bars.vb_empty[i], 1);
+    }
+    for (int t = 0; t < NQ; ++t) {
+      ptx::mbar_init(&bars.s_full[t], 1);
+      ptx::mbar_init(&bars.p_full[t], BM);
+      ptx::mbar_init(&bars.o_done[t], 1);
+    }
+    ptx::fence_barrier_init();
+  }
+  if (warp == 2) ptx::tmem_alloc(&bars.tmem_base, 512);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+  volatile int* abort_flag = &bars.abort_flag;
+
+  if (warp < 4) {
+    ptx::regs_dec<56>();
+    if (warp == 0) {
+      // ------------------------------------------------------------ producer
+      if (ptx::elect_one()) {
+        ptx::mbar_arrive_expect_tx(&bars.q_full, NQ * 2 * kChunk);
+        for (int t = 0; t < NQ; ++t) {
+          const int row = q_row0 + t * BM;
+          ptx::tma_load_4d(sm + kOffQn + t * kChunk, &tm_qn, &bars.q_full, 0, h, row, b);
+          ptx::tma_load_4d(sm + kOffQr + t * kChunk, &tm_qr, &bars.q_full, 0, h, row, b);
+        }
+        for (int j = 0; j < n_kv; ++j) {
+          const int s = j % kStages, ph = ((j / kStages) & 1) ^ 1, key0 = j * BN;
+          if (!ptx::mbar_wait(&bars.k_empty[s], ph, abort_flag, p.err)) break;
+          ptx::mbar_arrive_expect_tx(&bars.k_full[s], 2 * kChunk);
+          ptx::tma_load_4d(sm + kOffKn + s * kChunk, &tm_kn, &bars.k_full[s], 0, h, key0, b);
+          ptx::tma_load_3d(sm + kOffKr + s * kChunk, &tm_kr, &bars.k_full[s], 0, key0, b);
+          if (!ptx::mbar_wait(&bars.v8_empty[s], ph, abort_flag, p.err)) break;
+          ptx::mbar_arrive_expect_tx(&bars.v8_full[s], kChunk);
+          ptx::tma_load_4d(sm + kOffV8 + s * kChunk, &tm_v, &bars.v8_full[s], 0, h, key0, b);
+        }
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer
+      if (ptx::elect_one()) {
+        constexpr uint32_t kIdS8 = ptx::make_idesc(0, BM, BN, 0, 0);   // e4m3 x e4m3
+        constexpr uint32_t kIdS16 = ptx::make_idesc(1, BM, BN, 0, 0);  // bf16 rope
+        constexpr uint32_t kIdPV = ptx::make_idesc(1, BM, 128, 0, 1);
+        const uint32_t qn = ptx::smem_u32(sm + kOffQn), qr = ptx::smem_u32(sm + kOffQr);
+        const uint32_t kn = ptx::smem_u32(sm + kOffKn), kr = ptx::smem_u32(sm + kOffKr);
+        const uint32_t vb = ptx::smem_u32(sm + kOffVb);
+        bool ok = ptx::mbar_wait(&bars.q_conv, 0, abort_flag, p.err);
+        auto wait_k = [&](int j) {
+          return ptx::mbar_wait(&bars.k_conv[j % kStages], (j / kStages) & 1, abort_flag, p.err);
+        };
+        auto issue_s = [&](int t, int j) {
+          const int s = j % kStages;
+          const uint32_t d = tmem + t * BN;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {  // nope: K = 128 fp8 = 4 x 32
+            const uint64_t da = ptx::sw128_desc(qn + t * kChunk + k * 32, 16, 1024);
+            const uint64_t db = ptx::sw128_desc(kn + s * kChunk + k * 32, 16, 1024);
+            ptx::mma_f8_ss(d, da, db, kIdS8, k > 0);
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {  // rope: K = 64 bf16 = 4 x 16
+            const uint64_t da = ptx::sw128_desc(qr + t * kChunk + k * 32, 16, 1024);
+            const uint64_t db = ptx::sw128_desc(kr + s * kChunk + k * 32, 16, 1024);
+            ptx::mma_bf16_ss(d, da, db, kIdS16, 1);
+          }
+        };
+        auto issue_pv = [&](int t, int j) {
+          const uint32_t v = vb + (j % kStages) * 2 * kChunk;
+          const uint32_t d = tmem + 2 * BN + t * 128;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {  // high part of P'
+            const uint64_t db = ptx::sw128_desc(v + k * 2048, kChunk, 1024);
+            ptx::mma_bf16_ts(d, tmem + t * BN + k * 8, db, kIdPV, (j > 0 || k > 0) ? 1u : 0u);
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {  // low part of P'
+            const uint64_t db = ptx::sw128_desc(v + k * 2048, kChunk, 1024);
+            ptx::mma_bf16_ts(d, tmem + t * BN + 64 + k * 8, db, kIdPV, 1u);
+          }
+        };
+        if (ok && n_kv > 0 && (ok = wait_k(0))) {
+          ptx::tc_fence_after();
+          issue_s(0, 0);
+          ptx::mma_commit(&bars.s_full[0]);
+          issue_s(1, 0);
+          ptx::mma_commit(&bars.s_full[1]);
+          ptx::mma_commit(&bars.k_empty[0]);
+        }
+        for (int j = 0; ok && j < n_kv; ++j) {
+          const int s = j % kStages;
+          const bool more = j + 1 < n_kv;
+          if (!(ok = ptx::mbar_wait(&bars.vb_full[s], (j / kStages) & 1, abort_flag, p.err))) break;
+          if (!(ok = ptx::mbar_wait(&bars.p_full[0], j & 1, abort_flag, p.err))) break;
+          ptx::tc_fence_after();
+          issue_pv(0, j);
+          ptx::mma_commit(&bars.o_done[0]);
+          if (more) {
+            if (!(ok = wait_k(j + 1))) break;
+            ptx::tc_fence_after();
+            issue_s(0, j + 1);
+            ptx::mma_commit(&bars.s_full[0]);
+          }
+          if (!(ok = ptx::mbar_wait(&bars.p_full[1], j & 1, abort_flag, p.err))) break;
+          ptx::tc_fence_after();
+          issue_pv(1, j);
+          ptx::mma_commit(&bars.o_done[1]);
+          ptx::mma_commit(&bars.vb_empty[s]);
+          if (more) {
+            issue_s(1, j + 1);
+            ptx::mma_commit(&bars.s_full[1]);
+            ptx::mma_commit(&bars.k_empty[(j + 1) % kStages]);
+          }
+        }
+      }
+    } else {
+      // ------------------------------------------------------------ converters (64 threads)
+      const int ct = threadIdx.x - 64;
+      bool ok = ptx::mbar_wait(&bars.q_full, 0, abort_flag, p.err);
+      if (ok) {
+        // Q rope rows / q_scale (rows past S: leave as loaded, they are never stored)
+        for (int rr = ct; rr < NQ * BM; rr += kConvThreads) {
+          const int i = q_row0 + rr;
+          const float f = i < p.S ? 1.f / __ldg(p.q_scale + (size_t)b * p.S + i) : 1.f;
+          uint4* row = reinterpret_cast<uint4*>(sm + kOffQr + (rr / BM) * kChunk + (rr % BM) * 128);
+#pragma unroll
+          for (int x = 0; x < 8; ++x) {
+            uint4 w = row[x];
+            w.x = bf16x2_scale(w.x, f); w.y = bf16x2_scale(w.y, f);
+            w.z = bf16x2_scale(w.z, f); w.w = bf16x2_scale(w.w, f);
+            row[x] = w;
+          }
+        }
+        ptx::fence_proxy_async();
+        ptx::mbar_arrive(&bars.q_conv);
+      }
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int s = j % kStages, ph = (j / kStages) & 1, key0 = j * BN;
+        ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.k_full[s], ph, abort_flag, p.err));
+        if (!ok) break;
+        // K rope rows / k_scale; key scales into smem for the softmax
+        for (int rr = ct; rr < BN; rr += kConvThreads) {
+          const int key = key0 + rr;
+          const float ksv = key < p.S ? __ldg(p.k_scale + (size_t)b * p.S + key) : 1.f;
+          bars.ks[s][rr] = ksv;
+          const float f = 1.f / ksv;
+          uint4* row = reinterpret_cast<uint4*>(sm + kOffKr + s * kChunk + rr * 128);
+#pragma unroll
+          for (int x = 0; x < 8; ++x) {
+            uint4 w = row[x];
+            w.x = bf16x2_scale(w.x, f); w.y = bf16x2_scale(w.y, f);
+            w.z = bf16x2_scale(w.z, f); w.w = bf16x2_scale(w.w, f);
+            row[x] = w;
+          }
+        }
+        ptx::fence_proxy_async();
+        ptx::mbar_arrive(&bars.k_conv[s]);
+        // V8 (128 keys x 128 fp8, one swizzled 128-byte row per key) -> bf16 N-major tile
+        ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.v8_full[s], ph, abort_flag, p.err));
+        if (!ok) break;
+        ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.vb_empty[s], ph ^ 1, abort_flag, p.err));
+        if (!ok) break;
+        for (int rr = ct; rr < BN; rr += kConvThreads) {
+          const unsigned char* src = sm + kOffV8 + s * kChunk + rr * 128;
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {  // 16 fp8 values = logical 16-byte group g of the row
+            const uint4 raw = *reinterpret_cast<const uint4*>(src + ((g ^ (rr & 7)) << 4));
+            const uint8_t* by = reinterpret_cast<const uint8_t*>(&raw);
+            uint32_t w[8];
+#pragma unroll
+            for (int x = 0; x < 8; ++x) w[x] = ptx::pack_bf16x2(e4m3_to_f32(by[2 * x]), e4m3_to_f32(by[2 * x + 1]));
+            // columns 16g .. 16g+15 -> chunk (g / 4), logical groups 2(g%4) and 2(g%4)+1
+            unsigned char* dst = sm + kOffVb + s * 2 * kChunk + (g >> 2) * kChunk + rr * 128;
+            const int g0 = 2 * (g & 3);
+            *reinterpret_cast<uint4*>(dst + ((g0 ^ (rr & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(dst + (((g0 + 1) ^ (rr & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+          }
+        }
+        ptx::fence_proxy_async();
+        ptx::mbar_arrive(&bars.v8_empty[s]);
+        ptx::mbar_arrive(&bars.vb_full[s]);
+      }
+    }
+  } else {
+    // -------------------------------------------------------------- softmax warpgroups
+    ptx::regs_inc<224>();
+    const int t = (warp >> 2) - 1;
+    const int r = (warp & 3) * 32 + lane;
+    const int i = q_row0 + t * BM + r;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t s_addr = tmem + lane_off + t * BN;
+    const uint32_t o_addr = tmem + lane_off + 2 * BN + t * 128;
+    const float qsc = (i < p.S ? __ldg(p.q_scale + (size_t)b * p.S + i) : 1.f) * p.scale_log2;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.s_full[t], j & 1, abort_flag, p.err));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const float* ks = bars.ks[j % kStages];
+      float s[128];
+      {
+        uint32_t v[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          ptx::tmem_ld32(s_addr + c * 32, v);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int x = 0; x < 32; ++x) s[c * 32 + x] = __uint_as_float(v[x]) * (qsc * ks[c * 32 + x]);
+        }
+      }
+      const int key0 = j * BN;
+      const bool need_mask = (key0 + BN > p.S) || (p.causal && key0 + BN - 1 > q_row0 + t * BM);
+      if (need_mask) {
+        const int lim = p.causal ? min(i + 1, p.S) : p.S;
+#pragma unroll
+        for (int x = 0; x < 128; ++x)
+          if (key0 + x >= lim) s[x] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int x = 1; x < 128; ++x) mx = fmaxf(mx, s[x]);
+      float m_use = m;
+      if (j == 0) {
+        m_use = mx;
+      } else {
+        const bool grow = mx > m + 8.0f;
+        if (__any_sync(0xffffffffu, grow)) {
+          ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.o_done[t], (j - 1) & 1, abort_flag, p.err));
+          if (!ok) break;
+          ptx::tc_fence_after();
+          const float alpha = grow ? ptx::ex2(m - mx) : 1.f;
+          if (grow) m_use = mx;
+          uint32_t v[32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            ptx::tmem_ld32(o_addr + c * 32, v);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int x = 0; x < 32; ++x) v[x] = __float_as_uint(__uint_as_float(v[x]) * alpha);
+            ptx::tmem_st32(o_addr + c * 32, v);
+          }
+          l *= alpha;
+        }
+      }
+      m = m_use;
+      const float neg_m = -m;
+      float psum = 0.f;
+      uint32_t hi[32], lo[32];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+          const int k0 = c * 64 + 2 * x;
+          const float p0 = ptx::ex2(s[k0] + neg_m);
+          const float p1 = ptx::ex2(s[k0 + 1] + neg_m);
+          psum += p0 + p1;
+          const float a = p0 * ks[k0], bq = p1 * ks[k0 + 1];
+          const uint32_t hw = ptx::pack_bf16x2(a, bq);
+          hi[x] = hw;
+          lo[x] = ptx::pack_bf16x2(a - __uint_as_float(hw << 16), bq - __uint_as_float(hw & 0xffff0000u));
+        }
+        ptx::tmem_st32(s_addr + c * 32, hi);       // P' high part: columns 0..63
+        ptx::tmem_st32(s_addr + 64 + c * 32, lo);  // P' low part: columns 64..127
+      }
+      l += psum;
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&bars.p_full[t]);
+    }
+    if (ok && n_kv > 0 &&
+        __all_sync(0xffffffffu, ptx::mbar_wait(&bars.o_done[t], (n_kv - 1) & 1, abort_flag, p.err))) {
+      ptx::tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const bool store = i < p.S;
+      const size_t row_off = ((static_cast<size_t>(b) * p.S + i) * p.H + h) * 128;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        ptx::tmem_ld32(o_addr + c * 32, v);
+        ptx::tmem_ld_wait();
+        if (store) {
+          if (p.out_f32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + row_off + c * 32);
+#pragma unroll
+            for (int x = 0; x < 8; ++x)
+              dst[x] = make_float4(__uint_as_float(v[4 * x]) * inv, __uint_as_float(v[4 * x + 1]) * inv,
+                                   __uint_as_float(v[4 * x + 2]) * inv, __uint_as_float(v[4 * x + 3]) * inv);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + row_off + c * 32);
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              uint4 w;
+              w.x = ptx::pack_bf16x2(__uint_as_float(v[8 * x + 0]) * inv, __uint_as_float(v[8 * x + 1]) * inv);
+              w.y = ptx::pack_bf16x2(__uint_as_float(v[8 * x + 2]) * inv, __uint_as_float(v[8 * x + 3]) * inv);
+              w.z = ptx::pack_bf16x2(__uint_as_float(v[8 * x + 4]) * inv, __uint_as_float(v[8 * x + 5]) * inv);
+              w.w = ptx::pack_bf16x2(__uint_as_float(v[8 * x + 6]) * inv, __uint_as_float(v[8 * x + 7]) * inv);
+              dst[x] = w;
+            }
+          }
+        }
+      }
+      if (store)
+        p.lse[(static_cast<size_t>(b) * p.H + h) * p.S + i] =
+            l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace sm103_prefill_fp8
+
+cudaError_t encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* ptr,
+                              const uint64_t* dims, const uint64_t* strides, const uint32_t* box);
+
+cudaError_t launch_prefill_sm103_fp8(const void* q_nope, const void* q_rope, const void* k_nope,
+                                     const void* k_rope, const void* v, const float* q_scale,
+                                     const float* k_scale, void* out, float* lse, int B, int H,
+                                     int S, float softmax_scale, int causal, bool out_f32,
+                                     unsigned int* err, cudaStream_t stream) {
+  using namespace sm103_prefill_fp8;
+  CUtensorMap tqn, tqr, tkn, tkr, tv;
+  // fp8 [B,S,H,128]: one 128-byte box row per token
+  uint64_t n_dims[4] = {128, (uint64_t)H, (uint64_t)S, (uint64_t)B};
+  uint64_t n_str[3] = {128, (uint64_t)H * 128, (uint64_t)S * H * 128};
+  uint32_t n_box[4] = {128, 1, 128, 1};
+  // bf16 q_rope [B,S,H,64]
+  uint64_t r_dims[4] = {64, (uint64_t)H, (uint64_t)S, (uint64_t)B};
+  uint64_t r_str[3] = {128, (uint64_t)H * 128, (uint64_t)S * H * 128};
+  uint32_t r_box[4] = {64, 1, 128, 1};
+  // bf16 k_rope [B,S,64]
+  uint64_t kr_dims[3] = {64, (uint64_t)S, (uint64_t)B};
+  uint64_t kr_str[2] = {128, (uint64_t)S * 128};
+  uint32_t kr_box[3] = {64, 128, 1};
+  cudaError_t e;
+  if ((e = encode_tensor_map(&tqn, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, q_nope, n_dims, n_str, n_box)) != cudaSuccess ||
+      (e = encode_tensor_map(&tkn, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, k_nope, n_dims, n_str, n_box)) != cudaSuccess ||
+      (e = encode_tensor_map(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, v, n_dims, n_str, n_box)) != cudaSuccess ||
+      (e = encode_tensor_map(&tqr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, q_rope, r_dims, r_str, r_box)) != cudaSuccess ||
+      (e = encode_tensor_map(&tkr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k_rope, kr_dims, kr_str, kr_box)) != cudaSuccess)
+    return e;
+  Params p;
+  p.B = B;
+  p.H = H;
+  p.S = S;
+  p.causal = causal;
+  p.nrb = (S + NQ * BM - 1) / (NQ * BM);
+  p.out_f32 = out_f32 ? 1 : 0;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.q_scale = q_scale;
+  p.k_scale = k_scale;
+  p.out = out;
+  p.lse = lse;
+  p.err = err;
+  static bool ready = false;
+  if (!ready) {
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, prefill_fp8_kernel)) != cudaSuccess) return e;
+    if (fa.numRegs != 168) return cudaErrorInvalidDeviceFunction;  // setmaxnreg split
+    if ((e = cudaFuncSetAttribute(prefill_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kSmemAlloc)) != cudaSuccess)
+      return e;
+    ready = true;
+  }
+  const long long grid = (long long)B * H * p.nrb;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  prefill_fp8_kernel<<<(unsigned)grid, kThreads, kSmemAlloc, stream>>>(tqn, tqr, tkn, tkr, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -290,8 +290,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int x = 0; x < 32; ++x) {
           const float p0 = ptx::ex2(fmaf(s[c * 64 + 2 * x], p.scale_log2, neg_m));
           const float p1 = ptx::ex2(fmaf(s[c * 64 + 2 * x + 1], p.scale_log2, neg_m));
-          psum += p0 + p1;
-          pk[x] = ptx::pack_bf16x2(p0, p1);
+          // the row sum adds the bf16-rounded values the PV product actually uses, so a
+          // dominant key is normalised exactly
+          const uint32_t w = ptx::pack_bf16x2(p0, p1);
+          pk[x] = w;
+          psum += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
         }
         ptx::tmem_st32(s_addr + c * 32, pk);
       }
@@ -350,37 +353,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- host side
 
-namespace {
+cudaError_t encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* ptr,
+                              const uint64_t* dims, const uint64_t* strides, const uint32_t* box);
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    cudaDriverEntryPointQueryResult q;
-    void* p = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
+static bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* p,
+                   const uint64_t* dims, const uint64_t* strides, const uint32_t* box) {
+  return encode_tensor_map(m, dt, rank, p, dims, strides, box) == cudaSuccess;
 }
-
-// Tensor map over a row-major tensor given innermost-first dims and byte strides of
-// dims 1.., with a box of `box` elements per dim, 128-byte swizzle, zero fill outside.
-bool encode(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* ptr,
-            const uint64_t* dims, const uint64_t* strides, const uint32_t* box) {
-  auto fn = get_encoder();
-  if (!fn) return false;
-  cuuint32_t es[5] = {1, 1, 1, 1, 1};
-  CUresult r = fn(map, dt, rank, const_cast<void*>(ptr), reinterpret_cast<const cuuint64_t*>(dims),
-                  reinterpret_cast<const cuuint64_t*>(strides),
-                  reinterpret_cast<const cuuint32_t*>(box), es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
-}  // namespace
 
 // [B, S, H, d] tensor of 2-byte elements, box = 64 columns x 1 head x `rows` tokens
 static bool map_bshd(CUtensorMap* m, const void* p, int B, int S, int H, int d, int rows) {

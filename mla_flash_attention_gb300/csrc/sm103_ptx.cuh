@@ -58,25 +58,46 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with parity `parity` to complete.  Gives up after about
-// `limit_cycles` SM clocks, latches kErrTimeout in the device error word and sets the
-// CTA's abort flag; returns false in that case (and immediately if abort is set).
+// `limit_cycles` SM clocks (or as soon as any CTA of the launch has latched a timeout in
+// the device error word), latches kErrTimeout and sets the CTA's abort flag; returns false
+// in that case (and immediately if the abort flag is already set).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           unsigned int* err,
-                                          long long limit_cycles = 4000000000LL) {
+                                          long long limit_cycles = 1000000000LL) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  while (true) {
+  for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > limit_cycles) {
-      latch_error(err, kErrTimeout);
-      *abort_flag = 1;
-      return false;
+    if ((it & 1023u) == 0) {
+      const bool other = err && (*reinterpret_cast<volatile unsigned int*>(err) & kErrTimeout);
+      if (other || clock64() - t0 > limit_cycles) {
+        latch_error(err, kErrTimeout);
+        *abort_flag = 1;
+        return false;
+      }
     }
   }
 }
 
 // ------------------------------------------------------------------ TMA
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// Bring a 2-D box into L2 ahead of its load (no shared memory, no completion signal).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c0, int c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
 
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                             int c0, int c1, int c2) {
@@ -99,6 +120,12 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Make this thread's generic-proxy shared-memory writes visible to the async proxy
+// (TMA, tensor core operand reads).
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ tcgen05
