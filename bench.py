@@ -239,7 +239,7 @@ def run_gpu(args):
                    "l2": "inputs (1.6 GB) larger than L2; no flush",
                    "parallelism": "replicas (dp%d, no collective)" % world},
     }
-    src = ["prefill_simt.cu"]
+    src = ["prefill_sm103.cu", "sm103_ptx.cuh"]
     achieved = flops / (ms_mean * 1e-3) / 1e12
     res["roofline"] = {"kernel": "prefill", "bound": "tensor", "achieved": achieved,
                        "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
@@ -370,8 +370,45 @@ def run_reference(args):
     print(json.dumps(res))
 
 
+PROFILE_CASES = {
+    # reduced workloads for ncu captures: same shapes per (batch, head) / per sequence, a few
+    # hundred MB of inputs (larger than L2), 1 warm-up + 2 launches
+    "prefill": dict(kind="prefill", B=1, H=64, S=4096, fp8=False, seed=1001),
+    "prefill_fp8": dict(kind="prefill", B=1, H=64, S=8192, fp8=True, seed=1002),
+    "decode": dict(kind="decode", B=32, H=128, T=1, lens=4096, fp8=False, seed=1003),
+    "decode_fp8": dict(kind="decode", B=64, H=16, T=2, lens=("uniform", 1, 8192), fp8=True,
+                       seed=1004),
+}
+
+
+def run_profile_case(name):
+    """Run one reduced workload (for ncu); no timing, no JSON."""
+    import torch
+
+    from gen import make_decode, make_prefill
+    from mla_flash_attention_gb300 import binding
+    from mla_flash_attention_gb300.testing import decode_to_device, prefill_to_device
+
+    c = PROFILE_CASES[name]
+    dev = torch.device("cuda", 0)
+    if c["kind"] == "prefill":
+        inp = make_prefill(c["B"], c["H"], c["S"], fp8=c["fp8"], seed=c["seed"])
+        t = prefill_to_device(inp, dev)
+        for _ in range(3):
+            binding.mla_prefill(*t["args"], softmax_scale=inp.softmax_scale, causal=True)
+    else:
+        inp = make_decode(c["B"], c["H"], c["T"], c["lens"], fp8=c["fp8"], seed=c["seed"])
+        d = decode_to_device(inp, dev)
+        for _ in range(3):
+            binding.mla_decode(*d["args"], **d["kwargs"], softmax_scale=inp.softmax_scale)
+    torch.cuda.synchronize()
+    binding.check_device_error()
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--profile", choices=sorted(PROFILE_CASES),
+                    help="run one reduced workload for an ncu capture and exit")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
@@ -379,6 +416,9 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline prefill + bf16 decode only")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
+    if args.profile:
+        run_profile_case(args.profile)
+        return
     if args.impl == "ours":
         args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.impl == "reference":
