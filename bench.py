@@ -130,6 +130,47 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# --------------------------------------------------------------------------- ranks
+
+class Ranks:
+    """Whole-job aggregation over the ranks of a torchrun launch (or a single process).
+
+    Every rank runs an independent replica; the job's throughput is the work of all ranks
+    divided by the slowest rank's time.
+    """
+
+    def __init__(self, dist=None, device=None):
+        self.dist = dist
+        self.device = device
+
+    def _reduce(self, x, op):
+        if self.dist is None:
+            return float(x)
+        import torch
+
+        t = torch.tensor([float(x)], dtype=torch.float64, device=self.device)
+        self.dist.all_reduce(t, op=op)
+        return float(t.item())
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+        if self.device is not None and self.device.type == "cuda":
+            import torch
+
+            torch.cuda.synchronize(self.device)
+
+    def max(self, x):
+        return x if self.dist is None else self._reduce(x, self.dist.ReduceOp.MAX)
+
+    def sum(self, x):
+        return x if self.dist is None else self._reduce(x, self.dist.ReduceOp.SUM)
+
+    def rate(self, work_local, ms_local):
+        """(sum of work over ranks) / (max over ranks of the elapsed ms), per second."""
+        return self.sum(work_local) / (self.max(ms_local) * 1e-3)
+
+
 # --------------------------------------------------------------------------- GPU arm
 
 def time_calls(fn, steps, warmup, flush=None):
@@ -171,17 +212,8 @@ def run_gpu(args):
 
         dist.init_process_group("nccl", device_id=dev)
 
-    def barrier():
-        if dist is not None:
-            dist.barrier()
-        torch.cuda.synchronize()
-
-    def max_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    ranks = Ranks(dist, dev)
+    barrier, max_over_ranks = ranks.barrier, ranks.max
 
     pk = peaks()
     flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
@@ -230,7 +262,7 @@ def run_gpu(args):
     torch.cuda.empty_cache()
 
     res = {
-        "metric": METRIC, "value": world * flops / (ms_mean * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "metric": METRIC, "value": ranks.rate(flops, ms_mean) / 1e12, "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_mean,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: seeded PCG64 N(0,1) rounded to bf16 (no dataset)",
@@ -246,7 +278,7 @@ def run_gpu(args):
                        "frac": achieved / pk["bf16_tflops"],
                        "traffic": recorded_traffic("prefill_bf16", src),
                        "peak_source": pk["source"] + " (bf16 dense, burst; of measured)"}
-    res["e2e"] = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+    res["e2e"] = {"value": ranks.rate(flops, e2e_ms) / 1e12, "unit": "TFLOP/s",
                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
     res["clocks"] = clocks
 
