@@ -7,7 +7,7 @@
 // part) and their own half of O += P C[:, half].  Query rows are the (token, head) pairs
 // of one sequence, padded to the MMA's M = 128.
 //
-// Per CTA (12 warps):
+// Per CTA (8 warps):
 //   warp 0      TMA producer of cache pages (bf16 cache): 64 keys x 576 columns per stage
 //   warp 1      MMA issuer: S(g) = Q C(g)' into one of two S buffers (A operand = Q:
 //               latent 0..255 from TMEM, latent 256..511 + rope from shared memory),
@@ -36,7 +36,7 @@ constexpr int kOffQhi = 0;                    // latent 256..511 (4 chunks) + ro
 constexpr int kOffStage = 5 * kQChunk;        // 80 KB
 constexpr int kSmemBytes = kOffStage + kStages * kStageBytes;  // 224 KB
 constexpr int kSmemAlloc = kSmemBytes + 1024;
-constexpr int kThreads = 384;
+constexpr int kThreads = 256;
 constexpr int kPrepThreads = 64;
 
 struct Params {
@@ -139,7 +139,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   int seq, L, lo, hi;
 
   if (warp < 4) {
-    ptx::regs_dec<56>();
     if (warp == 0) {
       // ------------------------------------------------------------ TMA producer (bf16)
       if (!kFp8 && ptx::elect_one()) {
@@ -285,7 +284,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // -------------------------------------------------------------- softmax / Q / epilogue
-    ptx::regs_inc<224>();
     const int r = threadIdx.x - 128;  // query row == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int t_row = r / p.H;
@@ -324,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_arrive(&bars.q_ready);
       }
       const int last_visible = p.causal ? (L - p.T + t_row) : (L - 1);  // keys <= this are visible
-      float m = -INFINITY, l = 0.f;
+      float m = -INFINITY, l = 0.f, lr = 0.f;  // exact row sum (LSE) and bf16-rounded (PV)
       const uint32_t o_addr = tmem + lane_off + 256;
       for (int pg = lo; pg < hi; ++pg, ++g) {
         ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.s_full[g & 1], (g >> 1) & 1, abort_flag, p.err));
@@ -376,28 +374,31 @@ __global__ void __launch_bounds__(kThreads, 1)
               ptx::tmem_st32(o_addr + c * 32, v);
             }
             l *= alpha;
+            lr *= alpha;
           }
         }
         m = m_use;
         const float neg_m = (m == -INFINITY) ? 0.f : -m;
-        float psum = 0.f;
+        float psum = 0.f, prsum = 0.f;
         uint32_t pk[32];
 #pragma unroll
         for (int x = 0; x < 32; ++x) {
           const float p0 = ptx::ex2(s[2 * x] + neg_m);
           const float p1 = ptx::ex2(s[2 * x + 1] + neg_m);
+          psum += p0 + p1;
           if constexpr (kFp8) {
-            psum += p0 + p1;
             pk[x] = ptx::pack_bf16x2(p0 * bars.kscale[g % kStages][2 * x],
                                      p1 * bars.kscale[g % kStages][2 * x + 1]);
           } else {
-            // sum the bf16-rounded values the PV product uses (exact for a dominant key)
+            // O is normalised by the sum of the bf16-rounded values the PV product uses
+            // (exact for a dominant key); the LSE uses the exact sum
             const uint32_t w = ptx::pack_bf16x2(p0, p1);
             pk[x] = w;
-            psum += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+            prsum += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
           }
         }
         l += psum;
+        lr += kFp8 ? psum : prsum;
         ptx::tmem_st32(s_addr, pk);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
@@ -409,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       ptx::tc_fence_after();
       const size_t slot = (size_t)unit + seq;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = lr > 0.f ? 1.f / lr : 0.f;
       float* dst = p.part_o + (slot * TH + r) * kDl + half * 256;
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
@@ -483,11 +484,7 @@ cudaError_t launch_decode_sm103(const void* q_latent, const void* q_rope, const 
   auto go = [&](auto kern) -> cudaError_t {
     static bool checked[2] = {false, false};
     if (!checked[fp8 ? 1 : 0]) {
-      cudaFuncAttributes fa;
-      cudaError_t e = cudaFuncGetAttributes(&fa, kern);
-      if (e != cudaSuccess) return e;
-      if (fa.numRegs != 168) return cudaErrorInvalidDeviceFunction;  // setmaxnreg split
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
       if (e != cudaSuccess) return e;
       checked[fp8 ? 1 : 0] = true;
     }

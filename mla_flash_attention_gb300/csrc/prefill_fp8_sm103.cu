@@ -1,18 +1,19 @@
 // Fused MLA prefill with fp8 e4m3 Q_nope / K_nope / V and one fp32 scale per query and per
 // key token (tcgen05 + TMEM + TMA).
 //
-// Score: s_ij = scale * (qs_i ks_j (Qn8_i . Kn8_j) + Qr_i . Kr_j).  The per-token scales are
-// folded so that one fp32 accumulator serves both depths:
-//   acc_ij = Qn8_i . Kn8_j + (Qr_i / qs_i) . (Kr_j / ks_j),   s_ij = scale qs_i ks_j acc_ij,
-// with the nope product on the 8-bit MMA (kind::f8f6f4) and the rescaled rope product on the
-// bf16 MMA.  V_j = ks_j V8_j, so the PV product uses P'_ij = p_ij ks_j against V8 widened to
-// bf16 (exact); P' is split into a bf16 high part and a bf16 low part (two MMAs) so the
-// product keeps ~16 significant bits -- O reaches |O| ~ 40 on the fp8 workload and is
-// accumulated and written in fp32.
+// Score: s_ij = scale * (qs_i ks_j Sn_ij + Sr_ij) with Sn = Qn8 Kn8' on the 8-bit MMA
+// (kind::f8f6f4) and Sr = Qr Kr' on the bf16 MMA, accumulated in two separate fp32 TMEM
+// buffers (the scales are applied per element in the softmax, so nothing is rounded
+// before the fp32 sum).  V_j = ks_j V8_j, so the PV product uses P'_ij = p_ij ks_j against
+// V8 widened to bf16 (exact); P' is split into a bf16 high part and a bf16 low part (two
+// MMAs), keeping ~16 significant bits -- O reaches |O| ~ 40 on the fp8 workload and is
+// accumulated and (by default) written in fp32.
 //
-// Roles (12 warps): warp 0 TMA producer; warp 1 MMA issuer; warps 2-3 converters (rope
-// rescaling by 1/scale, V8 -> bf16 into a 128B-swizzled N-major tile, key scales into smem);
-// warps 4-7 / 8-11 softmax of Q tiles 0 / 1 (as in the bf16 kernel).
+// One CTA = (batch, head, 256 query rows as two 128-row tiles), keys in tiles of 64.  TMEM
+// per Q tile t: [t*256, +64) Sn (later P' high | P' low), [+64, +128) Sr, [+128, +256) O.
+// Roles (12 warps): warp 0 TMA producer (4-stage rings); warp 1 MMA issuer; warps 2-3
+// converters (V8 -> bf16 into a 128B-swizzled N-major tile, key scales into smem);
+// warps 4-7 / 8-11 softmax of Q tiles 0 / 1.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -22,16 +23,17 @@
 namespace mla {
 namespace sm103_prefill_fp8 {
 
-constexpr int BM = 128, BN = 128, NQ = 2;
-constexpr int kChunk = 128 * 128;          // 128 rows x 128 bytes
-constexpr int kStages = 2;
-constexpr int kOffQn = 0;                                  // NQ x 16 KB (fp8)
-constexpr int kOffQr = kOffQn + NQ * kChunk;               // NQ x 16 KB (bf16 rope / qs)
-constexpr int kOffKn = kOffQr + NQ * kChunk;               // stages x 16 KB
-constexpr int kOffKr = kOffKn + kStages * kChunk;          // stages x 16 KB
-constexpr int kOffV8 = kOffKr + kStages * kChunk;          // stages x 16 KB
-constexpr int kOffVb = kOffV8 + kStages * kChunk;          // stages x 32 KB
-constexpr int kSmemBytes = kOffVb + kStages * 2 * kChunk;  // 224 KB
+constexpr int BM = 128, BN = 64, NQ = 2;
+constexpr int kQChunk = BM * 128;          // 128 rows x 128 bytes
+constexpr int kKChunk = BN * 128;          // 64 rows x 128 bytes
+constexpr int kStages = 4;
+constexpr int kOffQn = 0;                                  // NQ x 16 KB (fp8 nope)
+constexpr int kOffQr = kOffQn + NQ * kQChunk;              // NQ x 16 KB (bf16 rope)
+constexpr int kOffKn = kOffQr + NQ * kQChunk;              // stages x 8 KB
+constexpr int kOffKr = kOffKn + kStages * kKChunk;         // stages x 8 KB
+constexpr int kOffV8 = kOffKr + kStages * kKChunk;         // stages x 8 KB
+constexpr int kOffVb = kOffV8 + kStages * kKChunk;         // stages x 16 KB (2 chunks)
+constexpr int kSmemBytes = kOffVb + kStages * 2 * kKChunk; // 64 + 160 = 224 KB
 constexpr int kSmemAlloc = kSmemBytes + 1024;
 constexpr int kThreads = 384;
 constexpr int kConvThreads = 64;
@@ -47,9 +49,10 @@ struct Params {
 };
 
 struct Bars {
-  uint64_t q_full, q_conv;
-  uint64_t k_full[kStages], k_conv[kStages], k_empty[kStages];
+  uint64_t q_full;
+  uint64_t k_full[kStages], k_empty[kStages];
   uint64_t v8_full[kStages], v8_empty[kStages], vb_full[kStages], vb_empty[kStages];
+  uint64_t ks_full[kStages];
   uint64_t s_full[NQ], p_full[NQ], o_done[NQ];
   uint32_t tmem_base;
   int abort_flag;
@@ -59,12 +62,6 @@ struct Bars {
 __device__ __forceinline__ int n_kv_tiles(const Params& p, int q_row0) {
   const int all = (p.S + BN - 1) / BN;
   return p.causal ? min(all, (q_row0 + NQ * BM + BN - 1) / BN) : all;
-}
-
-__device__ __forceinline__ uint32_t bf16x2_scale(uint32_t w, float f) {
-  const float lo = __uint_as_float(w << 16) * f;
-  const float hi = __uint_as_float(w & 0xffff0000u) * f;
-  return ptx::pack_bf16x2(lo, hi);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -89,15 +86,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     bars.abort_flag = 0;
     ptx::mbar_init(&bars.q_full, 1);
-    ptx::mbar_init(&bars.q_conv, kConvThreads);
     for (int i = 0; i < kStages; ++i) {
       ptx::mbar_init(&bars.k_full[i], 1);
-      ptx::mbar_init(&bars.k_conv[i], kConvThreads);
       ptx::mbar_init(&bars.k_empty[i], 1);
       ptx::mbar_init(&bars.v8_full[i], 1);
       ptx::mbar_init(&bars.v8_empty[i], kConvThreads);
       ptx::mbar_init(&bars.vb_full[i], kConvThreads);
       ptx::mbar_init(&bars.vb_empty[i], 1);
+      ptx::mbar_init(&bars.ks_full[i], kConvThreads);
     }
     for (int t = 0; t < NQ; ++t) {
       ptx::mbar_init(&bars.s_full[t], 1);
@@ -118,21 +114,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
       // ------------------------------------------------------------ producer
       if (ptx::elect_one()) {
-        ptx::mbar_arrive_expect_tx(&bars.q_full, NQ * 2 * kChunk);
+        ptx::mbar_arrive_expect_tx(&bars.q_full, NQ * 2 * kQChunk);
         for (int t = 0; t < NQ; ++t) {
           const int row = q_row0 + t * BM;
-          ptx::tma_load_4d(sm + kOffQn + t * kChunk, &tm_qn, &bars.q_full, 0, h, row, b);
-          ptx::tma_load_4d(sm + kOffQr + t * kChunk, &tm_qr, &bars.q_full, 0, h, row, b);
+          ptx::tma_load_4d(sm + kOffQn + t * kQChunk, &tm_qn, &bars.q_full, 0, h, row, b);
+          ptx::tma_load_4d(sm + kOffQr + t * kQChunk, &tm_qr, &bars.q_full, 0, h, row, b);
         }
         for (int j = 0; j < n_kv; ++j) {
           const int s = j % kStages, ph = ((j / kStages) & 1) ^ 1, key0 = j * BN;
           if (!ptx::mbar_wait(&bars.k_empty[s], ph, abort_flag, p.err)) break;
-          ptx::mbar_arrive_expect_tx(&bars.k_full[s], 2 * kChunk);
-          ptx::tma_load_4d(sm + kOffKn + s * kChunk, &tm_kn, &bars.k_full[s], 0, h, key0, b);
-          ptx::tma_load_3d(sm + kOffKr + s * kChunk, &tm_kr, &bars.k_full[s], 0, key0, b);
+          ptx::mbar_arrive_expect_tx(&bars.k_full[s], 2 * kKChunk);
+          ptx::tma_load_4d(sm + kOffKn + s * kKChunk, &tm_kn, &bars.k_full[s], 0, h, key0, b);
+          ptx::tma_load_3d(sm + kOffKr + s * kKChunk, &tm_kr, &bars.k_full[s], 0, key0, b);
           if (!ptx::mbar_wait(&bars.v8_empty[s], ph, abort_flag, p.err)) break;
-          ptx::mbar_arrive_expect_tx(&bars.v8_full[s], kChunk);
-          ptx::tma_load_4d(sm + kOffV8 + s * kChunk, &tm_v, &bars.v8_full[s], 0, h, key0, b);
+          ptx::mbar_arrive_expect_tx(&bars.v8_full[s], kKChunk);
+          ptx::tma_load_4d(sm + kOffV8 + s * kKChunk, &tm_v, &bars.v8_full[s], 0, h, key0, b);
         }
       }
     } else if (warp == 1) {
@@ -144,38 +140,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t qn = ptx::smem_u32(sm + kOffQn), qr = ptx::smem_u32(sm + kOffQr);
         const uint32_t kn = ptx::smem_u32(sm + kOffKn), kr = ptx::smem_u32(sm + kOffKr);
         const uint32_t vb = ptx::smem_u32(sm + kOffVb);
-        bool ok = ptx::mbar_wait(&bars.q_conv, 0, abort_flag, p.err);
+        bool ok = ptx::mbar_wait(&bars.q_full, 0, abort_flag, p.err);
         auto wait_k = [&](int j) {
-          return ptx::mbar_wait(&bars.k_conv[j % kStages], (j / kStages) & 1, abort_flag, p.err);
+          return ptx::mbar_wait(&bars.k_full[j % kStages], (j / kStages) & 1, abort_flag, p.err);
         };
         auto issue_s = [&](int t, int j) {
           const int s = j % kStages;
-          const uint32_t d = tmem + t * BN;
+          const uint32_t dn = tmem + t * 256, dr = dn + 64;
 #pragma unroll
           for (int k = 0; k < 4; ++k) {  // nope: K = 128 fp8 = 4 x 32
-            const uint64_t da = ptx::sw128_desc(qn + t * kChunk + k * 32, 16, 1024);
-            const uint64_t db = ptx::sw128_desc(kn + s * kChunk + k * 32, 16, 1024);
-            ptx::mma_f8_ss(d, da, db, kIdS8, k > 0);
+            const uint64_t da = ptx::sw128_desc(qn + t * kQChunk + k * 32, 16, 1024);
+            const uint64_t db = ptx::sw128_desc(kn + s * kKChunk + k * 32, 16, 1024);
+            ptx::mma_f8_ss(dn, da, db, kIdS8, k > 0);
           }
 #pragma unroll
           for (int k = 0; k < 4; ++k) {  // rope: K = 64 bf16 = 4 x 16
-            const uint64_t da = ptx::sw128_desc(qr + t * kChunk + k * 32, 16, 1024);
-            const uint64_t db = ptx::sw128_desc(kr + s * kChunk + k * 32, 16, 1024);
-            ptx::mma_bf16_ss(d, da, db, kIdS16, 1);
+            const uint64_t da = ptx::sw128_desc(qr + t * kQChunk + k * 32, 16, 1024);
+            const uint64_t db = ptx::sw128_desc(kr + s * kKChunk + k * 32, 16, 1024);
+            ptx::mma_bf16_ss(dr, da, db, kIdS16, k > 0);
           }
         };
         auto issue_pv = [&](int t, int j) {
-          const uint32_t v = vb + (j % kStages) * 2 * kChunk;
-          const uint32_t d = tmem + 2 * BN + t * 128;
+          const uint32_t v = vb + (j % kStages) * 2 * kKChunk;
+          const uint32_t d = tmem + t * 256 + 128;
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {  // high part of P'
-            const uint64_t db = ptx::sw128_desc(v + k * 2048, kChunk, 1024);
-            ptx::mma_bf16_ts(d, tmem + t * BN + k * 8, db, kIdPV, (j > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < 4; ++k) {  // high part of P': columns 0..31
+            const uint64_t db = ptx::sw128_desc(v + k * 2048, kKChunk, 1024);
+            ptx::mma_bf16_ts(d, tmem + t * 256 + k * 8, db, kIdPV, (j > 0 || k > 0) ? 1u : 0u);
           }
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {  // low part of P'
-            const uint64_t db = ptx::sw128_desc(v + k * 2048, kChunk, 1024);
-            ptx::mma_bf16_ts(d, tmem + t * BN + 64 + k * 8, db, kIdPV, 1u);
+          for (int k = 0; k < 4; ++k) {  // low part of P': columns 32..63
+            const uint64_t db = ptx::sw128_desc(v + k * 2048, kKChunk, 1024);
+            ptx::mma_bf16_ts(d, tmem + t * 256 + 32 + k * 8, db, kIdPV, 1u);
           }
         };
         if (ok && n_kv > 0 && (ok = wait_k(0))) {
@@ -214,66 +210,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else {
       // ------------------------------------------------------------ converters (64 threads)
-      const int ct = threadIdx.x - 64;
-      bool ok = ptx::mbar_wait(&bars.q_full, 0, abort_flag, p.err);
-      if (ok) {
-        // Q rope rows / q_scale (rows past S: leave as loaded, they are never stored)
-        for (int rr = ct; rr < NQ * BM; rr += kConvThreads) {
-          const int i = q_row0 + rr;
-          const float f = i < p.S ? 1.f / __ldg(p.q_scale + (size_t)b * p.S + i) : 1.f;
-          uint4* row = reinterpret_cast<uint4*>(sm + kOffQr + (rr / BM) * kChunk + (rr % BM) * 128);
-#pragma unroll
-          for (int x = 0; x < 8; ++x) {
-            uint4 w = row[x];
-            w.x = bf16x2_scale(w.x, f); w.y = bf16x2_scale(w.y, f);
-            w.z = bf16x2_scale(w.z, f); w.w = bf16x2_scale(w.w, f);
-            row[x] = w;
-          }
-        }
-        ptx::fence_proxy_async();
-        ptx::mbar_arrive(&bars.q_conv);
-      }
+      const int ct = threadIdx.x - 64;  // one key row each
+      bool ok = true;
       for (int j = 0; ok && j < n_kv; ++j) {
-        const int s = j % kStages, ph = (j / kStages) & 1, key0 = j * BN;
-        ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.k_full[s], ph, abort_flag, p.err));
-        if (!ok) break;
-        // K rope rows / k_scale; key scales into smem for the softmax
-        for (int rr = ct; rr < BN; rr += kConvThreads) {
-          const int key = key0 + rr;
-          const float ksv = key < p.S ? __ldg(p.k_scale + (size_t)b * p.S + key) : 1.f;
-          bars.ks[s][rr] = ksv;
-          const float f = 1.f / ksv;
-          uint4* row = reinterpret_cast<uint4*>(sm + kOffKr + s * kChunk + rr * 128);
-#pragma unroll
-          for (int x = 0; x < 8; ++x) {
-            uint4 w = row[x];
-            w.x = bf16x2_scale(w.x, f); w.y = bf16x2_scale(w.y, f);
-            w.z = bf16x2_scale(w.z, f); w.w = bf16x2_scale(w.w, f);
-            row[x] = w;
-          }
-        }
-        ptx::fence_proxy_async();
-        ptx::mbar_arrive(&bars.k_conv[s]);
-        // V8 (128 keys x 128 fp8, one swizzled 128-byte row per key) -> bf16 N-major tile
-        ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.v8_full[s], ph, abort_flag, p.err));
-        if (!ok) break;
+        const int s = j % kStages, ph = (j / kStages) & 1, key = j * BN + ct;
+        // slot s is free once PV(j - kStages) is done (which needed that tile's softmax)
         ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.vb_empty[s], ph ^ 1, abort_flag, p.err));
         if (!ok) break;
-        for (int rr = ct; rr < BN; rr += kConvThreads) {
-          const unsigned char* src = sm + kOffV8 + s * kChunk + rr * 128;
+        bars.ks[s][ct] = key < p.S ? __ldg(p.k_scale + (size_t)b * p.S + key) : 0.f;
+        ptx::mbar_arrive(&bars.ks_full[s]);
+        // V8 (64 keys x 128 fp8, one swizzled 128-byte row per key) -> bf16 N-major tile
+        ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.v8_full[s], ph, abort_flag, p.err));
+        if (!ok) break;
+        const unsigned char* src = sm + kOffV8 + s * kKChunk + ct * 128;
 #pragma unroll
-          for (int g = 0; g < 8; ++g) {  // 16 fp8 values = logical 16-byte group g of the row
-            const uint4 raw = *reinterpret_cast<const uint4*>(src + ((g ^ (rr & 7)) << 4));
-            const uint8_t* by = reinterpret_cast<const uint8_t*>(&raw);
-            uint32_t w[8];
+        for (int g = 0; g < 8; ++g) {  // 16 fp8 values = logical 16-byte group g of the row
+          const uint4 raw = *reinterpret_cast<const uint4*>(src + ((g ^ (ct & 7)) << 4));
+          const uint8_t* by = reinterpret_cast<const uint8_t*>(&raw);
+          uint32_t w[8];
 #pragma unroll
-            for (int x = 0; x < 8; ++x) w[x] = ptx::pack_bf16x2(e4m3_to_f32(by[2 * x]), e4m3_to_f32(by[2 * x + 1]));
-            // columns 16g .. 16g+15 -> chunk (g / 4), logical groups 2(g%4) and 2(g%4)+1
-            unsigned char* dst = sm + kOffVb + s * 2 * kChunk + (g >> 2) * kChunk + rr * 128;
-            const int g0 = 2 * (g & 3);
-            *reinterpret_cast<uint4*>(dst + ((g0 ^ (rr & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-            *reinterpret_cast<uint4*>(dst + (((g0 + 1) ^ (rr & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
-          }
+          for (int x = 0; x < 8; ++x)
+            w[x] = ptx::pack_bf16x2(e4m3_to_f32(by[2 * x]), e4m3_to_f32(by[2 * x + 1]));
+          // columns 16g .. 16g+15 -> chunk (g / 4), logical groups 2(g%4) and 2(g%4)+1
+          unsigned char* dst = sm + kOffVb + s * 2 * kKChunk + (g >> 2) * kKChunk + ct * 128;
+          const int g0 = 2 * (g & 3);
+          *reinterpret_cast<uint4*>(dst + ((g0 ^ (ct & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(dst + (((g0 + 1) ^ (ct & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
         }
         ptx::fence_proxy_async();
         ptx::mbar_arrive(&bars.v8_empty[s]);
@@ -287,25 +249,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = (warp & 3) * 32 + lane;
     const int i = q_row0 + t * BM + r;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t s_addr = tmem + lane_off + t * BN;
-    const uint32_t o_addr = tmem + lane_off + 2 * BN + t * 128;
-    const float qsc = (i < p.S ? __ldg(p.q_scale + (size_t)b * p.S + i) : 1.f) * p.scale_log2;
+    const uint32_t sn_addr = tmem + lane_off + t * 256;
+    const uint32_t o_addr = sn_addr + 128;
+    const float qs = i < p.S ? __ldg(p.q_scale + (size_t)b * p.S + i) : 1.f;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.s_full[t], j & 1, abort_flag, p.err));
       if (!ok) break;
       ptx::tc_fence_after();
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.ks_full[j % kStages], (j / kStages) & 1, abort_flag, p.err));
+      if (!ok) break;
       const float* ks = bars.ks[j % kStages];
-      float s[128];
+      float s[64];
       {
-        uint32_t v[32];
+        uint32_t vn[32], vr[32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          ptx::tmem_ld32(s_addr + c * 32, v);
+        for (int c = 0; c < 2; ++c) {
+          ptx::tmem_ld32(sn_addr + c * 32, vn);
+          ptx::tmem_ld32(sn_addr + 64 + c * 32, vr);
           ptx::tmem_ld_wait();
 #pragma unroll
-          for (int x = 0; x < 32; ++x) s[c * 32 + x] = __uint_as_float(v[x]) * (qsc * ks[c * 32 + x]);
+          for (int x = 0; x < 32; ++x)
+            s[c * 32 + x] = fmaf(__uint_as_float(vn[x]), qs * ks[c * 32 + x], __uint_as_float(vr[x])) *
+                            p.scale_log2;
         }
       }
       const int key0 = j * BN;
@@ -313,12 +280,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (need_mask) {
         const int lim = p.causal ? min(i + 1, p.S) : p.S;
 #pragma unroll
-        for (int x = 0; x < 128; ++x)
+        for (int x = 0; x < 64; ++x)
           if (key0 + x >= lim) s[x] = -INFINITY;
       }
       float mx = s[0];
 #pragma unroll
-      for (int x = 1; x < 128; ++x) mx = fmaxf(mx, s[x]);
+      for (int x = 1; x < 64; ++x) mx = fmaxf(mx, s[x]);
       float m_use = m;
       if (j == 0) {
         m_use = mx;
@@ -343,25 +310,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       m = m_use;
-      const float neg_m = -m;
+      const float neg_m = (m == -INFINITY) ? 0.f : -m;
       float psum = 0.f;
       uint32_t hi[32], lo[32];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-#pragma unroll
-        for (int x = 0; x < 32; ++x) {
-          const int k0 = c * 64 + 2 * x;
-          const float p0 = ptx::ex2(s[k0] + neg_m);
-          const float p1 = ptx::ex2(s[k0 + 1] + neg_m);
-          psum += p0 + p1;
-          const float a = p0 * ks[k0], bq = p1 * ks[k0 + 1];
-          const uint32_t hw = ptx::pack_bf16x2(a, bq);
-          hi[x] = hw;
-          lo[x] = ptx::pack_bf16x2(a - __uint_as_float(hw << 16), bq - __uint_as_float(hw & 0xffff0000u));
-        }
-        ptx::tmem_st32(s_addr + c * 32, hi);       // P' high part: columns 0..63
-        ptx::tmem_st32(s_addr + 64 + c * 32, lo);  // P' low part: columns 64..127
+      for (int x = 0; x < 32; ++x) {
+        const float p0 = ptx::ex2(s[2 * x] + neg_m);
+        const float p1 = ptx::ex2(s[2 * x + 1] + neg_m);
+        psum += p0 + p1;
+        const float a = p0 * ks[2 * x], bq = p1 * ks[2 * x + 1];
+        const uint32_t hw = ptx::pack_bf16x2(a, bq);
+        hi[x] = hw;
+        lo[x] = ptx::pack_bf16x2(a - __uint_as_float(hw << 16), bq - __uint_as_float(hw & 0xffff0000u));
       }
+      ptx::tmem_st32(sn_addr, hi);       // P' high part: columns 0..31
+      ptx::tmem_st32(sn_addr + 32, lo);  // P' low part: columns 32..63
       l += psum;
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
@@ -424,22 +387,23 @@ cudaError_t launch_prefill_sm103_fp8(const void* q_nope, const void* q_rope, con
                                      unsigned int* err, cudaStream_t stream) {
   using namespace sm103_prefill_fp8;
   CUtensorMap tqn, tqr, tkn, tkr, tv;
-  // fp8 [B,S,H,128]: one 128-byte box row per token
+  // fp8 [B,S,H,128]: one 128-byte box row per token (Q: 128 tokens per box, K/V: 64)
   uint64_t n_dims[4] = {128, (uint64_t)H, (uint64_t)S, (uint64_t)B};
   uint64_t n_str[3] = {128, (uint64_t)H * 128, (uint64_t)S * H * 128};
-  uint32_t n_box[4] = {128, 1, 128, 1};
+  uint32_t q_box[4] = {128, 1, BM, 1};
+  uint32_t k_box[4] = {128, 1, BN, 1};
   // bf16 q_rope [B,S,H,64]
   uint64_t r_dims[4] = {64, (uint64_t)H, (uint64_t)S, (uint64_t)B};
   uint64_t r_str[3] = {128, (uint64_t)H * 128, (uint64_t)S * H * 128};
-  uint32_t r_box[4] = {64, 1, 128, 1};
+  uint32_t r_box[4] = {64, 1, BM, 1};
   // bf16 k_rope [B,S,64]
   uint64_t kr_dims[3] = {64, (uint64_t)S, (uint64_t)B};
   uint64_t kr_str[2] = {128, (uint64_t)S * 128};
-  uint32_t kr_box[3] = {64, 128, 1};
+  uint32_t kr_box[3] = {64, BN, 1};
   cudaError_t e;
-  if ((e = encode_tensor_map(&tqn, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, q_nope, n_dims, n_str, n_box)) != cudaSuccess ||
-      (e = encode_tensor_map(&tkn, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, k_nope, n_dims, n_str, n_box)) != cudaSuccess ||
-      (e = encode_tensor_map(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, v, n_dims, n_str, n_box)) != cudaSuccess ||
+  if ((e = encode_tensor_map(&tqn, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, q_nope, n_dims, n_str, q_box)) != cudaSuccess ||
+      (e = encode_tensor_map(&tkn, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, k_nope, n_dims, n_str, k_box)) != cudaSuccess ||
+      (e = encode_tensor_map(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, v, n_dims, n_str, k_box)) != cudaSuccess ||
       (e = encode_tensor_map(&tqr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, q_rope, r_dims, r_str, r_box)) != cudaSuccess ||
       (e = encode_tensor_map(&tkr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k_rope, kr_dims, kr_str, kr_box)) != cudaSuccess)
     return e;

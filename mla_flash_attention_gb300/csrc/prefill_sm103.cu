@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t s_addr = tmem + lane_off + t * BN;
     const uint32_t o_addr = tmem + lane_off + 2 * BN + t * 128;
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY, l = 0.f, lr = 0.f;  // exact row sum (LSE), bf16-rounded sum (O)
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.s_full[t], j & 1, abort_flag, p.err));
@@ -278,11 +278,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_st32(o_addr + c * 32, v);
           }
           l *= alpha;
+          lr *= alpha;
         }
       }
       m = m_use;
       const float neg_m = -m;
-      float psum = 0.f;
+      float psum = 0.f, prsum = 0.f;
       uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
@@ -290,15 +291,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int x = 0; x < 32; ++x) {
           const float p0 = ptx::ex2(fmaf(s[c * 64 + 2 * x], p.scale_log2, neg_m));
           const float p1 = ptx::ex2(fmaf(s[c * 64 + 2 * x + 1], p.scale_log2, neg_m));
-          // the row sum adds the bf16-rounded values the PV product actually uses, so a
-          // dominant key is normalised exactly
+          // O is normalised by the sum of the bf16-rounded values the PV product uses (so a
+          // dominant key is normalised exactly); the LSE uses the exact sum
           const uint32_t w = ptx::pack_bf16x2(p0, p1);
           pk[x] = w;
-          psum += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+          psum += p0 + p1;
+          prsum += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
         }
         ptx::tmem_st32(s_addr + c * 32, pk);
       }
       l += psum;
+      lr += prsum;
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       ptx::mbar_arrive(&bars.p_full[t]);
@@ -307,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && n_kv > 0 &&
         __all_sync(0xffffffffu, ptx::mbar_wait(&bars.o_done[t], (n_kv - 1) & 1, abort_flag, p.err))) {
       ptx::tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = lr > 0.f ? 1.f / lr : 0.f;
       const bool store = i < p.S;
       const size_t row_off = ((static_cast<size_t>(b) * p.S + i) * p.H + h) * 128;
 #pragma unroll
