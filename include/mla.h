@@ -120,6 +120,34 @@ mla_status mla_decode(const void* q_latent, const void* q_rope, const void* kv_c
                       size_t workspace_bytes, void* stream);
 
 /*
+ * mla_decode_noalloc -- mla_decode for callers that cannot allocate device memory.
+ * (This entry point has no counterpart in the source pages: it exists for callers that run
+ * where cudaMalloc and other allocating calls are not allowed -- e.g. an inference engine
+ * that owns all device memory from start-up, or a plugin hook that may not allocate -- and
+ * therefore cannot supply mla_decode's workspace.)
+ *
+ * Arguments, layouts and results are those of mla_decode without the workspace: the split
+ * partials go to a scratch array compiled into the library, of
+ * mla_decode_noalloc_max_workspace() bytes (48 MiB), which every GPU that loads the library
+ * holds until the process exits.  Allocates nothing.
+ *   - A batch whose mla_decode_workspace_size() exceeds that size is rejected with
+ *     MLA_ERR_WORKSPACE before anything is launched.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress);
+ *     make that first call before any stream capture.
+ *   - All calls on a device share the array, which keeps the last call's contents (nothing
+ *     needs clearing: a call only reads what it wrote).  Calls that overlap on the GPU race
+ *     on the array; the caller must serialise them (one stream, or ordered streams).
+ */
+mla_status mla_decode_noalloc(const void* q_latent, const void* q_rope, const void* kv_cache,
+                              const float* kv_scale, const int* page_table, const int* cache_lens,
+                              void* out, float* lse, int B, int H, int q_len, int d_latent,
+                              int d_rope, int page_size, int max_pages_per_seq, int num_pages,
+                              float softmax_scale, int causal, mla_dtype kv_dtype, void* stream);
+
+/* Bytes of the built-in scratch array used by mla_decode_noalloc. */
+size_t mla_decode_noalloc_max_workspace(void);
+
+/*
  * mla_check_device_error -- synchronise `stream`, then read and clear the device
  * error word latched by earlier kernels of this library on the current device.
  * Returns MLA_OK, MLA_ERR_TIMEOUT or MLA_ERR_DEVICE_CHECK (or MLA_ERR_CUDA if the

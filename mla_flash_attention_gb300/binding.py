@@ -36,6 +36,11 @@ _lib.mla_decode_workspace_size.argtypes = [_i, _i, _i, _i]
 _lib.mla_decode.restype = _i
 _lib.mla_decode.argtypes = [_vp, _vp, _vp, _fp, _ip, _ip, _vp, _fp, _i, _i, _i, _i, _i, _i, _i, _i,
                             _f, _i, _i, _vp, _sz, _vp]
+_lib.mla_decode_noalloc.restype = _i
+_lib.mla_decode_noalloc.argtypes = [_vp, _vp, _vp, _fp, _ip, _ip, _vp, _fp, _i, _i, _i, _i, _i, _i,
+                                    _i, _i, _f, _i, _i, _vp]
+_lib.mla_decode_noalloc_max_workspace.restype = _sz
+_lib.mla_decode_noalloc_max_workspace.argtypes = []
 _lib.mla_check_device_error.restype = _i
 _lib.mla_check_device_error.argtypes = [_vp]
 _lib.mla_last_error.restype = ctypes.c_char_p
@@ -43,7 +48,8 @@ _lib.mla_last_error.argtypes = []
 _lib.mla_version.restype = _i
 _lib.mla_version.argtypes = []
 
-EXPORTED = ("mla_prefill", "mla_decode_workspace_size", "mla_decode", "mla_check_device_error",
+EXPORTED = ("mla_prefill", "mla_decode_workspace_size", "mla_decode", "mla_decode_noalloc",
+            "mla_decode_noalloc_max_workspace", "mla_check_device_error",
             "mla_last_error", "mla_version")
 
 
@@ -178,5 +184,46 @@ def mla_decode(q_latent, q_rope, kv_cache, page_table, cache_lens, kv_scale=None
                          dr, page_size, max_pages, num_pages, float(softmax_scale),
                          int(bool(causal)), MLA_FP8_E4M3 if fp8 else MLA_BF16, _ptr(workspace),
                          workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st)
+    return out, lse
+
+
+def decode_noalloc_max_workspace() -> int:
+    return int(_lib.mla_decode_noalloc_max_workspace())
+
+
+def mla_decode_noalloc(q_latent, q_rope, kv_cache, page_table, cache_lens, kv_scale=None, *,
+                       softmax_scale: float, causal: bool = True, out=None, lse=None, stream=None):
+    """mla_decode without a workspace: for callers that cannot allocate device memory at
+    call time.  The split partials use the library's built-in scratch array (see
+    include/mla.h); calls on one device must not overlap on the GPU.  ``out``/``lse`` may
+    be passed in so that the call itself allocates nothing."""
+    B, T, H, dl = q_latent.shape
+    dr = q_rope.shape[-1]
+    num_pages, page_size, _ = kv_cache.shape
+    fp8 = kv_cache.dtype == torch.float8_e4m3fn
+    _need(q_latent, "q_latent", torch.bfloat16, (B, T, H, dl))
+    _need(q_rope, "q_rope", torch.bfloat16, (B, T, H, dr))
+    _need(kv_cache, "kv_cache", torch.float8_e4m3fn if fp8 else torch.bfloat16,
+          (num_pages, page_size, dl + dr))
+    if fp8:
+        _need(kv_scale, "kv_scale", torch.float32, (num_pages, page_size))
+    elif kv_scale is not None:
+        raise ValueError("kv_scale is only used with an fp8 cache")
+    max_pages = page_table.shape[1]
+    _need(page_table, "page_table", torch.int32, (B, max_pages))
+    _need(cache_lens, "cache_lens", torch.int32, (B,))
+    dev = q_latent.device
+    if out is None:
+        out = torch.empty((B, T, H, dl), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.bfloat16, (B, T, H, dl))
+    _need(lse, "lse", torch.float32, (B, H, T))
+    st = _lib.mla_decode_noalloc(_ptr(q_latent), _ptr(q_rope), _ptr(kv_cache), _ptr(kv_scale),
+                                 _ptr(page_table), _ptr(cache_lens), _ptr(out), _ptr(lse), B, H, T,
+                                 dl, dr, page_size, max_pages, num_pages, float(softmax_scale),
+                                 int(bool(causal)), MLA_FP8_E4M3 if fp8 else MLA_BF16,
+                                 _stream(stream))
     _check(st)
     return out, lse

@@ -12,11 +12,6 @@
 #include "common.cuh"
 
 namespace mla {
-cudaError_t launch_prefill_simt(const void* q_nope, const void* q_rope, const void* k_nope,
-                                const void* k_rope, const void* v, const float* q_scale,
-                                const float* k_scale, void* out, float* lse, int B, int H,
-                                int S, float softmax_scale, int causal, bool fp8, bool out_f32,
-                                cudaStream_t stream);
 cudaError_t launch_prefill_sm103_bf16(const void* q_nope, const void* q_rope, const void* k_nope,
                                       const void* k_rope, const void* v, void* out, float* lse,
                                       int B, int H, int S, float softmax_scale, int causal,
@@ -103,6 +98,19 @@ DecodeWorkspace decode_workspace_layout(void* base, int B, int TH, int d_latent,
 }
 
 }  // namespace
+
+namespace mla {
+// Records `fmt` as this thread's last-error message (for entry points in other files).
+mla_status set_last_error(mla_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+}  // namespace mla
 
 extern "C" {
 
