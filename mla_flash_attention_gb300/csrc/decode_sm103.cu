@@ -331,28 +331,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t s_addr = tmem + lane_off + 128 + (g & 1) * 64;
         float s[64];
         {
-          uint32_t v[32];
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            ptx::tmem_ld32(s_addr + c * 32, v);
-            ptx::tmem_ld_wait();
-#pragma unroll
-            for (int x = 0; x < 32; ++x) s[c * 32 + x] = __uint_as_float(v[x]);
-          }
+          uint32_t* su = reinterpret_cast<uint32_t*>(s);
+          ptx::tmem_ld32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(su));
+          ptx::tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(su + 32));
+          ptx::tmem_ld_wait();
         }
         const int page = __ldg(p.page_table + (size_t)seq * p.max_pages + pg);
         const bool bad = page < 0 || page >= p.num_pages;
         const int key0 = pg * kPage;
         const int lim = bad ? -1 : min(last_visible, L - 1);  // visible keys: key0+x <= lim
-        float mx = -INFINITY;
+        float mx8[8] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY,
+                        -INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int x = 0; x < 64; ++x) {
           float v = s[x];
           if constexpr (kFp8) v *= bars.kscale[g % kStages][x];
           v = (key0 + x <= lim) ? v * p.scale_log2 : -INFINITY;
           s[x] = v;
-          mx = fmaxf(mx, v);
+          mx8[x & 7] = fmaxf(mx8[x & 7], v);
         }
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         float m_use = m;
         if (pg == lo) {
           m_use = mx;
@@ -379,13 +378,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         m = m_use;
         const float neg_m = (m == -INFINITY) ? 0.f : -m;
-        float psum = 0.f, prsum = 0.f;
+        float ps[4] = {0.f, 0.f, 0.f, 0.f}, pr[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t pk[32];
 #pragma unroll
         for (int x = 0; x < 32; ++x) {
           const float p0 = ptx::ex2(s[2 * x] + neg_m);
           const float p1 = ptx::ex2(s[2 * x + 1] + neg_m);
-          psum += p0 + p1;
+          ps[x & 3] += p0 + p1;
           if constexpr (kFp8) {
             pk[x] = ptx::pack_bf16x2(p0 * bars.kscale[g % kStages][2 * x],
                                      p1 * bars.kscale[g % kStages][2 * x + 1]);
@@ -394,11 +393,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // (exact for a dominant key); the LSE uses the exact sum
             const uint32_t w = ptx::pack_bf16x2(p0, p1);
             pk[x] = w;
-            prsum += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+            pr[x & 3] += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
           }
         }
+        const float psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
         l += psum;
-        lr += kFp8 ? psum : prsum;
+        lr += kFp8 ? psum : (pr[0] + pr[1]) + (pr[2] + pr[3]);
         ptx::tmem_st32(s_addr, pk);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();

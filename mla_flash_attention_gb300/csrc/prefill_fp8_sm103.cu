@@ -82,6 +82,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = bh / p.H, h = bh % p.H;
   const int q_row0 = rb * NQ * BM;
   const int n_kv = n_kv_tiles(p, q_row0);
+  // causal: Q tile 0 never sees the key tiles past its own rows (above the diagonal)
+  const int n_kv0 = p.causal ? min(n_kv, (q_row0 + BM + BN - 1) / BN) : n_kv;
 
   if (threadIdx.x == 0) {
     bars.abort_flag = 0;
@@ -185,16 +187,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; ok && j < n_kv; ++j) {
           const int s = j % kStages;
           const bool more = j + 1 < n_kv;
+          bool k_ready = false;
           if (!(ok = ptx::mbar_wait(&bars.vb_full[s], (j / kStages) & 1, abort_flag, p.err))) break;
-          if (!(ok = ptx::mbar_wait(&bars.p_full[0], j & 1, abort_flag, p.err))) break;
-          ptx::tc_fence_after();
-          issue_pv(0, j);
-          ptx::mma_commit(&bars.o_done[0]);
-          if (more) {
-            if (!(ok = wait_k(j + 1))) break;
+          if (j < n_kv0) {
+            if (!(ok = ptx::mbar_wait(&bars.p_full[0], j & 1, abort_flag, p.err))) break;
             ptx::tc_fence_after();
-            issue_s(0, j + 1);
-            ptx::mma_commit(&bars.s_full[0]);
+            issue_pv(0, j);
+            ptx::mma_commit(&bars.o_done[0]);
+            if (j + 1 < n_kv0) {
+              if (!(ok = wait_k(j + 1))) break;
+              k_ready = true;
+              ptx::tc_fence_after();
+              issue_s(0, j + 1);
+              ptx::mma_commit(&bars.s_full[0]);
+            }
           }
           if (!(ok = ptx::mbar_wait(&bars.p_full[1], j & 1, abort_flag, p.err))) break;
           ptx::tc_fence_after();
@@ -202,6 +208,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mma_commit(&bars.o_done[1]);
           ptx::mma_commit(&bars.vb_empty[s]);
           if (more) {
+            if (!k_ready && !(ok = wait_k(j + 1))) break;
+            ptx::tc_fence_after();
             issue_s(1, j + 1);
             ptx::mma_commit(&bars.s_full[1]);
             ptx::mma_commit(&bars.k_empty[(j + 1) % kStages]);
@@ -254,7 +262,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float qs = i < p.S ? __ldg(p.q_scale + (size_t)b * p.S + i) : 1.f;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
+    const int n_t = t == 0 ? n_kv0 : n_kv;  // key tiles this Q tile sees
+    for (int j = 0; j < n_t; ++j) {
       ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.s_full[t], j & 1, abort_flag, p.err));
       if (!ok) break;
       ptx::tc_fence_after();
@@ -283,9 +292,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int x = 0; x < 64; ++x)
           if (key0 + x >= lim) s[x] = -INFINITY;
       }
-      float mx = s[0];
+      float mx8[8];
 #pragma unroll
-      for (int x = 1; x < 64; ++x) mx = fmaxf(mx, s[x]);
+      for (int q = 0; q < 8; ++q) mx8[q] = s[q];
+#pragma unroll
+      for (int x = 8; x < 64; ++x) mx8[x & 7] = fmaxf(mx8[x & 7], s[x]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       float m_use = m;
       if (j == 0) {
         m_use = mx;
@@ -311,13 +324,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       m = m_use;
       const float neg_m = (m == -INFINITY) ? 0.f : -m;
-      float psum = 0.f;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t hi[32], lo[32];
 #pragma unroll
       for (int x = 0; x < 32; ++x) {
         const float p0 = ptx::ex2(s[2 * x] + neg_m);
         const float p1 = ptx::ex2(s[2 * x + 1] + neg_m);
-        psum += p0 + p1;
+        ps[x & 3] += p0 + p1;
         const float a = p0 * ks[2 * x], bq = p1 * ks[2 * x + 1];
         const uint32_t hw = ptx::pack_bf16x2(a, bq);
         hi[x] = hw;
@@ -325,13 +338,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::tmem_st32(sn_addr, hi);       // P' high part: columns 0..31
       ptx::tmem_st32(sn_addr + 32, lo);  // P' low part: columns 32..63
-      l += psum;
+      l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       ptx::mbar_arrive(&bars.p_full[t]);
     }
-    if (ok && n_kv > 0 &&
-        __all_sync(0xffffffffu, ptx::mbar_wait(&bars.o_done[t], (n_kv - 1) & 1, abort_flag, p.err))) {
+    if (ok && n_t > 0 &&
+        __all_sync(0xffffffffu, ptx::mbar_wait(&bars.o_done[t], (n_t - 1) & 1, abort_flag, p.err))) {
       ptx::tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const bool store = i < p.S;

@@ -76,6 +76,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = bh / p.H, h = bh % p.H;
   const int q_row0 = rb * NQ * BM;
   const int n_kv = n_kv_tiles(p, q_row0);
+  // causal: Q tile 0 never sees the last key tile of its row block (all of it is above the
+  // diagonal), so its S / softmax / PV stop one tile earlier
+  const int n_kv0 = p.causal ? min(n_kv, (q_row0 + BM + BN - 1) / BN) : n_kv;
 
   if (threadIdx.x == 0) {
     bars.abort_flag = 0;
@@ -196,14 +199,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int vseq = 2 * j + 1;
         if (!(ok = ptx::mbar_wait(&bars.ring_full[vseq % kRingSlots], (vseq / kRingSlots) & 1, abort_flag, p.err))) break;
         const bool more = j + 1 < n_kv;
-        if (!(ok = ptx::mbar_wait(&bars.p_full[0], j & 1, abort_flag, p.err))) break;
-        ptx::tc_fence_after();
-        issue_pv(0, j);
-        ptx::mma_commit(&bars.o_done[0]);
-        if (more) {
-          if (!(ok = wait_k(j + 1))) break;
-          issue_s(0, j + 1);
-          ptx::mma_commit(&bars.s_full[0]);
+        bool k_ready = false;
+        if (j < n_kv0) {
+          if (!(ok = ptx::mbar_wait(&bars.p_full[0], j & 1, abort_flag, p.err))) break;
+          ptx::tc_fence_after();
+          issue_pv(0, j);
+          ptx::mma_commit(&bars.o_done[0]);
+          if (j + 1 < n_kv0) {
+            if (!(ok = wait_k(j + 1))) break;
+            k_ready = true;
+            issue_s(0, j + 1);
+            ptx::mma_commit(&bars.s_full[0]);
+          }
         }
         if (!(ok = ptx::mbar_wait(&bars.p_full[1], j & 1, abort_flag, p.err))) break;
         ptx::tc_fence_after();
@@ -211,6 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mma_commit(&bars.o_done[1]);
         ptx::mma_commit(&bars.ring_empty[vseq % kRingSlots]);
         if (more) {
+          if (!k_ready && !(ok = wait_k(j + 1))) break;
           issue_s(1, j + 1);
           ptx::mma_commit(&bars.s_full[1]);
           ptx::mma_commit(&bars.ring_empty[(2 * j + 2) % kRingSlots]);
@@ -229,20 +237,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t o_addr = tmem + lane_off + 2 * BN + t * 128;
     float m = -INFINITY, l = 0.f, lr = 0.f;  // exact row sum (LSE), bf16-rounded sum (O)
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
+    const int n_t = t == 0 ? n_kv0 : n_kv;  // key tiles this Q tile sees
+    for (int j = 0; j < n_t; ++j) {
       ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.s_full[t], j & 1, abort_flag, p.err));
       if (!ok) break;
       ptx::tc_fence_after();
       float s[128];
       {
-        uint32_t v[32];
+        // all four 32-column loads in flight before one wait
+        uint32_t* su = reinterpret_cast<uint32_t*>(s);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          ptx::tmem_ld32(s_addr + c * 32, v);
-          ptx::tmem_ld_wait();
-#pragma unroll
-          for (int x = 0; x < 32; ++x) s[c * 32 + x] = __uint_as_float(v[x]);
-        }
+        for (int c = 0; c < 4; ++c)
+          ptx::tmem_ld32(s_addr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(su + c * 32));
+        ptx::tmem_ld_wait();
       }
       const int key0 = j * BN;
       const bool need_mask = (key0 + BN > p.S) || (p.causal && key0 + BN - 1 > q_row0 + t * BM);
@@ -252,9 +259,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int x = 0; x < 128; ++x)
           if (key0 + x >= lim) s[x] = -INFINITY;
       }
-      float mx = s[0];
+      // row max as 8 independent chains (few warps per scheduler: latency is not hidden)
+      float mx8[8];
 #pragma unroll
-      for (int x = 1; x < 128; ++x) mx = fmaxf(mx, s[x]);
+      for (int q = 0; q < 8; ++q) mx8[q] = s[q];
+#pragma unroll
+      for (int x = 8; x < 128; ++x) mx8[x & 7] = fmaxf(mx8[x & 7], s[x]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_tile = mx * p.scale_log2;  // -inf stays -inf
       float m_use = m;
       if (j == 0) {
@@ -268,14 +280,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tc_fence_after();
           const float alpha = grow ? ptx::ex2(m - m_tile) : 1.f;
           if (grow) m_use = m_tile;
-          uint32_t v[32];
+          uint32_t v[2][32];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            ptx::tmem_ld32(o_addr + c * 32, v);
+          for (int c = 0; c < 4; c += 2) {
+            ptx::tmem_ld32(o_addr + c * 32, v[0]);
+            ptx::tmem_ld32(o_addr + (c + 1) * 32, v[1]);
             ptx::tmem_ld_wait();
 #pragma unroll
-            for (int x = 0; x < 32; ++x) v[x] = __float_as_uint(__uint_as_float(v[x]) * alpha);
-            ptx::tmem_st32(o_addr + c * 32, v);
+            for (int x = 0; x < 32; ++x) {
+              v[0][x] = __float_as_uint(__uint_as_float(v[0][x]) * alpha);
+              v[1][x] = __float_as_uint(__uint_as_float(v[1][x]) * alpha);
+            }
+            ptx::tmem_st32(o_addr + c * 32, v[0]);
+            ptx::tmem_st32(o_addr + (c + 1) * 32, v[1]);
           }
           l *= alpha;
           lr *= alpha;
@@ -283,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       m = m_use;
       const float neg_m = -m;
-      float psum = 0.f, prsum = 0.f;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f}, pr[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
@@ -295,20 +312,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           // dominant key is normalised exactly); the LSE uses the exact sum
           const uint32_t w = ptx::pack_bf16x2(p0, p1);
           pk[x] = w;
-          psum += p0 + p1;
-          prsum += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+          ps[x & 3] += p0 + p1;
+          pr[x & 3] += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
         }
         ptx::tmem_st32(s_addr + c * 32, pk);
       }
-      l += psum;
-      lr += prsum;
+      l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+      lr += (pr[0] + pr[1]) + (pr[2] + pr[3]);
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       ptx::mbar_arrive(&bars.p_full[t]);
     }
     // epilogue: O / l -> out, LSE
-    if (ok && n_kv > 0 &&
-        __all_sync(0xffffffffu, ptx::mbar_wait(&bars.o_done[t], (n_kv - 1) & 1, abort_flag, p.err))) {
+    if (ok && n_t > 0 &&
+        __all_sync(0xffffffffu, ptx::mbar_wait(&bars.o_done[t], (n_t - 1) & 1, abort_flag, p.err))) {
       ptx::tc_fence_after();
       const float inv = lr > 0.f ? 1.f / lr : 0.f;
       const bool store = i < p.S;
