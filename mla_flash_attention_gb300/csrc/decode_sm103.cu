@@ -8,12 +8,15 @@
 // of one sequence, padded to the MMA's M = 128.
 //
 // Per CTA (8 warps):
-//   warp 0      TMA producer of cache pages (bf16 cache): 64 keys x 576 columns per stage
+//   warp 0      TMA producer: one cache page (64 keys x 576 columns) per stage, as nine
+//               64-column chunks -- bf16: 128B-swizzled, ready for the MMA; fp8: raw bytes
+//               into the upper half of the stage -- plus L2 prefetch of pages ahead
 //   warp 1      MMA issuer: S(g) = Q C(g)' into one of two S buffers (A operand = Q:
-//               latent 0..255 from TMEM, latent 256..511 + rope from shared memory),
-//               then O_half += P(g) C(g)[:, half] with P read from TMEM
-//   warps 2-3   stage preparation: zero the rows past the sequence end of a partial page
-//               (bf16), or load + convert an fp8 page to bf16 and stage its row scales
+//               latent 0..255 from TMEM, latent 256..511 + rope from shared memory), then
+//               O_half += P(g) C(g)[:, half] with P read from TMEM.  S(g+1) and PV(g) are
+//               issued in whichever order their inputs arrive.
+//   warps 2-3   stage preparation: zero the rows past the sequence end of a partial page;
+//               fp8: widen the page to bf16 in place (chunk by chunk) and stage its scales
 //   warps 4-7   softmax, one thread per query row; they also load each sequence's Q and
 //               write the split's partial (O_half / l, log-sum-exp)
 // TMEM columns: [0,128) Q latent 0..255 (bf16 pairs), [128,256) two S / P buffers of 64,
@@ -30,6 +33,8 @@ namespace sm103_decode {
 constexpr int kPage = 64, kDl = 512, kDc = 576, kRows = 128;
 constexpr int kPageChunk = kPage * 128;       // 64 rows x 64 bf16 (8 KB), 128B-swizzled
 constexpr int kStageBytes = 9 * kPageChunk;   // 72 KB
+constexpr int kRawChunk = kPage * 64;         // 64 rows x 64 fp8 bytes (4 KB), unswizzled
+constexpr int kRawOffset = 9 * kRawChunk;     // fp8 page lands in the upper 36 KB of a stage
 constexpr int kStages = 2;
 constexpr int kQChunk = kRows * 128;          // 128 rows x 64 bf16 (16 KB)
 constexpr int kOffQhi = 0;                    // latent 256..511 (4 chunks) + rope (1 chunk)
@@ -38,11 +43,11 @@ constexpr int kSmemBytes = kOffStage + kStages * kStageBytes;  // 224 KB
 constexpr int kSmemAlloc = kSmemBytes + 1024;
 constexpr int kThreads = 256;
 constexpr int kPrepThreads = 64;
+constexpr int kPrefetchAhead = 4;             // pages warmed in L2 ahead of their load
 
 struct Params {
   const uint16_t* q_latent;  // [B, T, H, 512]
   const uint16_t* q_rope;    // [B, T, H, 64]
-  const uint8_t* cache8;     // fp8 cache [num_pages, 64, 576] (fp8 path)
   const float* kv_scale;     // [num_pages, 64] (fp8 path)
   const int* page_table;
   const int* cache_lens;
@@ -55,7 +60,7 @@ struct Params {
 
 struct Bars {
   uint64_t stage_full[kStages], stage_ready[kStages], stage_empty[kStages];
-  uint64_t s_full[2], p_full[2], o_done, q_ready;
+  uint64_t s_full[2], p_full[2], o_done, q_ready, conv_sync;
   uint32_t tmem_base;
   int abort_flag;
   float kscale[kStages][kPage];
@@ -68,13 +73,14 @@ __device__ __forceinline__ int clamp_len(int L, int max_pages) {
 // Walks the (sequence, page range) segments of this CTA's work unit in order; every
 // role runs its own copy and sees the same sequence.
 struct Segments {
-  const Params* p;
-  int start, end;  // flat page range
-  int b, pb;       // current sequence and its first flat page
+  const int* lens;
+  int B, max_pages, start, end, b, pb;
   __device__ void init(const Params& prm, int unit) {
-    p = &prm;
+    lens = prm.cache_lens;
+    B = prm.B;
+    max_pages = prm.max_pages;
     int total = 0;
-    for (int i = 0; i < prm.B; ++i) total += pages_of(clamp_len(__ldg(prm.cache_lens + i), prm.max_pages), kPage);
+    for (int i = 0; i < B; ++i) total += pages_of(clamp_len(__ldg(lens + i), max_pages), kPage);
     const int chunk = total > 0 ? (total + prm.G - 1) / prm.G : 1;
     start = unit * chunk;
     end = min(total, start + chunk);
@@ -83,8 +89,8 @@ struct Segments {
   }
   // Next non-empty segment: sets seq, L, lo, hi (page indices within the sequence).
   __device__ bool next(int& seq, int& L, int& lo, int& hi) {
-    while (b < p->B && pb < end) {
-      const int Lb = clamp_len(__ldg(p->cache_lens + b), p->max_pages);
+    while (b < B && pb < end) {
+      const int Lb = clamp_len(__ldg(lens + b), max_pages);
       const int n = pages_of(Lb, kPage);
       const int l0 = max(start, pb) - pb, h0 = min(end, pb + n) - pb;
       const int cur = b;
@@ -102,6 +108,12 @@ struct Segments {
   }
 };
 
+__device__ __forceinline__ int page_row(const Params& p, int seq, int pg) {
+  const int page = __ldg(p.page_table + (size_t)seq * p.max_pages + pg);
+  // an out-of-range page reads as zeros (coordinates outside the tensor) and is masked
+  return (page >= 0 && page < p.num_pages) ? page * kPage : -2 * kPage;
+}
+
 template <bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_cache, const Params p) {
@@ -109,7 +121,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   __shared__ Bars bars;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
   const int unit = blockIdx.x >> 1, half = blockIdx.x & 1;
   const int TH = p.T * p.H;
 
@@ -126,6 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::mbar_init(&bars.o_done, 1);
     ptx::mbar_init(&bars.q_ready, kRows);
+    ptx::mbar_init(&bars.conv_sync, kPrepThreads);
     ptx::fence_barrier_init();
   }
   if (warp == 2) ptx::tmem_alloc(&bars.tmem_base, 512);
@@ -138,148 +151,173 @@ __global__ void __launch_bounds__(kThreads, 1)
   segs.init(p, unit);
   int seq, L, lo, hi;
 
-  if (warp < 4) {
-    if (warp == 0) {
-      // ------------------------------------------------------------ TMA producer (bf16)
-      if (!kFp8 && ptx::elect_one()) {
-        int g = 0;
-        bool ok = true;
-        while (ok && segs.next(seq, L, lo, hi)) {
-          for (int pg = lo; pg < hi; ++pg, ++g) {
-            const int s = g % kStages;
-            if (!(ok = ptx::mbar_wait(&bars.stage_empty[s], ((g / kStages) & 1) ^ 1, abort_flag, p.err))) break;
-            const int page = __ldg(p.page_table + (size_t)seq * p.max_pages + pg);
-            // an out-of-range page reads as zeros (outside the tensor) and is masked later
-            const int y = (page >= 0 && page < p.num_pages) ? page * kPage : -2 * kPage;
-            unsigned char* dst = sm + kOffStage + s * kStageBytes;
-            ptx::mbar_arrive_expect_tx(&bars.stage_full[s], kStageBytes);
-#pragma unroll 1
-            for (int c = 0; c < 9; ++c)
-              ptx::tma_load_2d(dst + c * kPageChunk, &tm_cache, &bars.stage_full[s], c * 64, y);
-            // warm L2 with the page two steps ahead of this one (same sequence only)
-            if (half == 0 && pg + 2 < hi) {
-              const int ahead = __ldg(p.page_table + (size_t)seq * p.max_pages + pg + 2);
-              if (ahead >= 0 && ahead < p.num_pages)
-#pragma unroll 1
-                for (int c = 0; c < 9; ++c) ptx::tma_prefetch_2d(&tm_cache, c * 64, ahead * kPage);
-            }
-          }
-        }
-      }
-    } else if (warp == 1) {
-      // ------------------------------------------------------------ MMA issuer
-      if (ptx::elect_one()) {
-        constexpr uint32_t kIdS = ptx::make_idesc(1, kRows, kPage, 0, 0);
-        constexpr uint32_t kIdPV = ptx::make_idesc(1, kRows, 256, 0, 1);
-        const uint32_t qhi = ptx::smem_u32(sm + kOffQhi);
-        const uint32_t stage0 = ptx::smem_u32(sm + kOffStage);
-        const uint32_t o_tm = tmem + 256;
-        int g = 0, nseg = 0;
-        bool ok = true;
-        auto issue_s = [&](int gg) {
-          const uint32_t st = stage0 + (gg % kStages) * kStageBytes;
-          const uint32_t d = tmem + 128 + (gg & 1) * 64;
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {  // latent 0..255: A from TMEM
-            const uint64_t db = ptx::sw128_desc(st + (k >> 2) * kPageChunk + (k & 3) * 32, 16, 1024);
-            ptx::mma_bf16_ts(d, tmem + k * 8, db, kIdS, k > 0);
-          }
-#pragma unroll
-          for (int k = 16; k < 36; ++k) {  // latent 256..511 + rope: A from shared memory
-            const int kq = k - 16;
-            const uint64_t da = ptx::sw128_desc(qhi + (kq >> 2) * kQChunk + (kq & 3) * 32, 16, 1024);
-            const uint64_t db = ptx::sw128_desc(st + (k >> 2) * kPageChunk + (k & 3) * 32, 16, 1024);
-            ptx::mma_bf16_ss(d, da, db, kIdS, 1);
-          }
-        };
-        while (ok && segs.next(seq, L, lo, hi)) {
-          // Q of this sequence (TMEM + shared memory) is written by the softmax warps
-          if (!(ok = ptx::mbar_wait(&bars.q_ready, nseg & 1, abort_flag, p.err))) break;
-          ptx::tc_fence_after();
-          const int n = hi - lo, g0 = g;
-          if (!(ok = ptx::mbar_wait(&bars.stage_ready[g0 % kStages], (g0 / kStages) & 1, abort_flag, p.err))) break;
-          ptx::tc_fence_after();
-          issue_s(g0);
-          ptx::mma_commit(&bars.s_full[g0 & 1]);
-          for (int i = 0; i < n; ++i, ++g) {
-            if (i + 1 < n) {
-              const int g1 = g + 1;
-              if (!(ok = ptx::mbar_wait(&bars.stage_ready[g1 % kStages], (g1 / kStages) & 1, abort_flag, p.err))) break;
-              ptx::tc_fence_after();
-              issue_s(g1);
-              ptx::mma_commit(&bars.s_full[g1 & 1]);
-            }
-            if (!(ok = ptx::mbar_wait(&bars.p_full[g & 1], (g >> 1) & 1, abort_flag, p.err))) break;
-            ptx::tc_fence_after();
-            const uint32_t st = stage0 + (g % kStages) * kStageBytes + 4 * half * kPageChunk;
-            const uint32_t pa = tmem + 128 + (g & 1) * 64;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint64_t db = ptx::sw128_desc(st + k * 2048, kPageChunk, 1024);
-              ptx::mma_bf16_ts(o_tm, pa + k * 8, db, kIdPV, (i > 0 || k > 0) ? 1u : 0u);
-            }
-            ptx::mma_commit(&bars.o_done);
-            ptx::mma_commit(&bars.stage_empty[g % kStages]);
-          }
-          ++nseg;
-        }
-      }
-    } else {
-      // ------------------------------------------------------------ stage preparation
-      const int tid = threadIdx.x - 64;  // 0..63
+  if (warp == 0) {
+    // -------------------------------------------------------------- TMA producer
+    if (ptx::elect_one()) {
+      ptx::prefetch_tensormap(&tm_cache);
       int g = 0;
       bool ok = true;
+      const int chunk_bytes = kFp8 ? kRawChunk : kPageChunk;
       while (ok && segs.next(seq, L, lo, hi)) {
+        for (int a = lo; a < min(hi, lo + kPrefetchAhead); ++a) {
+          const int y = page_row(p, seq, a);
+          if (y >= 0)
+            for (int c = 0; c < 9; ++c) ptx::tma_prefetch_2d(&tm_cache, c * 64, y);
+        }
         for (int pg = lo; pg < hi; ++pg, ++g) {
+          if (pg + kPrefetchAhead < hi) {
+            const int ya = page_row(p, seq, pg + kPrefetchAhead);
+            if (ya >= 0)
+              for (int c = 0; c < 9; ++c) ptx::tma_prefetch_2d(&tm_cache, c * 64, ya);
+          }
           const int s = g % kStages;
-          unsigned char* st = sm + kOffStage + s * kStageBytes;
-          const int valid = min(kPage, L - pg * kPage);  // rows holding tokens of this sequence
-          const int page = __ldg(p.page_table + (size_t)seq * p.max_pages + pg);
-          const bool bad = page < 0 || page >= p.num_pages;
-          if (bad && tid == 0) latch_error(p.err, kErrBadPage);
-          if constexpr (!kFp8) {
-            ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.stage_full[s], (g / kStages) & 1, abort_flag, p.err));
-            if (!ok) break;
-            if (valid < kPage) {
-              // zero rows valid..63 of all 9 chunks (16-byte granules)
-              const int nrow = kPage - valid;
-              for (int e = tid; e < nrow * 9 * 8; e += kPrepThreads) {
-                const int row = valid + e / 72, rem = e % 72, c = rem >> 3, gr = rem & 7;
-                *reinterpret_cast<uint4*>(st + c * kPageChunk + row * 128 + gr * 16) = make_uint4(0, 0, 0, 0);
-              }
-            }
-          } else {
-            ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.stage_empty[s], ((g / kStages) & 1) ^ 1, abort_flag, p.err));
-            if (!ok) break;
-            // 64 rows x 576 fp8 -> bf16, row-swizzled chunks; one thread per row
-            const int row = tid;
-            const bool live = !bad && row < valid;
-            const uint8_t* src = p.cache8 + ((size_t)(bad ? 0 : page) * kPage + row) * kDc;
-            bars.kscale[s][row] = live ? __ldg(p.kv_scale + (size_t)page * kPage + row) : 0.f;
-#pragma unroll 1
-            for (int c = 0; c < 9; ++c) {
-              uint4 raw[4];
+          if (!(ok = ptx::mbar_wait(&bars.stage_empty[s], ((g / kStages) & 1) ^ 1, abort_flag, p.err))) break;
+          const int y = page_row(p, seq, pg);
+          unsigned char* dst = sm + kOffStage + s * kStageBytes + (kFp8 ? kRawOffset : 0);
+          ptx::mbar_arrive_expect_tx(&bars.stage_full[s], 9 * chunk_bytes);
+          for (int c = 0; c < 9; ++c)
+            ptx::tma_load_2d(dst + c * chunk_bytes, &tm_cache, &bars.stage_full[s], c * 64, y);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------------- MMA issuer
+    if (ptx::elect_one()) {
+      constexpr uint32_t kIdS = ptx::make_idesc(1, kRows, kPage, 0, 0);
+      constexpr uint32_t kIdPV = ptx::make_idesc(1, kRows, 256, 0, 1);
+      const uint32_t qhi = ptx::smem_u32(sm + kOffQhi);
+      const uint32_t stage0 = ptx::smem_u32(sm + kOffStage);
+      const uint32_t o_tm = tmem + 256;
+      int g = 0, nseg = 0;
+      bool ok = true;
+      auto issue_s = [&](int gg) {
+        const uint32_t st = stage0 + (gg % kStages) * kStageBytes;
+        const uint32_t d = tmem + 128 + (gg & 1) * 64;
 #pragma unroll
-              for (int x = 0; x < 4; ++x)
-                raw[x] = live ? __ldg(reinterpret_cast<const uint4*>(src + c * 64) + x) : make_uint4(0, 0, 0, 0);
-              const uint8_t* bytes = reinterpret_cast<const uint8_t*>(raw);
-              unsigned char* dst = st + c * kPageChunk + row * 128;
+        for (int k = 0; k < 16; ++k) {  // latent 0..255: A from TMEM
+          const uint64_t db = ptx::sw128_desc(st + (k >> 2) * kPageChunk + (k & 3) * 32, 16, 1024);
+          ptx::mma_bf16_ts(d, tmem + k * 8, db, kIdS, k > 0);
+        }
 #pragma unroll
-              for (int gr = 0; gr < 8; ++gr) {
-                uint32_t w[4];
+        for (int k = 16; k < 36; ++k) {  // latent 256..511 + rope: A from shared memory
+          const int kq = k - 16;
+          const uint64_t da = ptx::sw128_desc(qhi + (kq >> 2) * kQChunk + (kq & 3) * 32, 16, 1024);
+          const uint64_t db = ptx::sw128_desc(st + (k >> 2) * kPageChunk + (k & 3) * 32, 16, 1024);
+          ptx::mma_bf16_ss(d, da, db, kIdS, 1);
+        }
+      };
+      auto issue_pv = [&](int gg, bool first) {
+        const uint32_t st = stage0 + (gg % kStages) * kStageBytes + 4 * half * kPageChunk;
+        const uint32_t pa = tmem + 128 + (gg & 1) * 64;
 #pragma unroll
-                for (int x = 0; x < 4; ++x) {
-                  const float a = e4m3_to_f32(bytes[gr * 8 + 2 * x]);
-                  const float bq = e4m3_to_f32(bytes[gr * 8 + 2 * x + 1]);
-                  w[x] = ptx::pack_bf16x2(a, bq);
-                }
-                *reinterpret_cast<uint4*>(dst + ((gr ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-              }
+        for (int k = 0; k < 4; ++k) {
+          const uint64_t db = ptx::sw128_desc(st + k * 2048, kPageChunk, 1024);
+          ptx::mma_bf16_ts(o_tm, pa + k * 8, db, kIdPV, (!first || k > 0) ? 1u : 0u);
+        }
+      };
+      while (ok && segs.next(seq, L, lo, hi)) {
+        // Q of this sequence (TMEM + shared memory) is written by the softmax warps
+        if (!(ok = ptx::mbar_wait(&bars.q_ready, nseg & 1, abort_flag, p.err))) break;
+        ptx::tc_fence_after();
+        const int g_end = g + (hi - lo), g_first = g;
+        int gs = g, gp = g;  // next page whose S / whose PV is to be issued
+        long long t0 = clock64();
+        while (gp < g_end) {
+          bool progress = false;
+          // S(gs) may run at most one page ahead of the oldest unissued PV (two S buffers)
+          if (gs < g_end && gs <= gp + 1 &&
+              ptx::mbar_test_wait(&bars.stage_ready[gs % kStages], (gs / kStages) & 1)) {
+            ptx::tc_fence_after();
+            issue_s(gs);
+            ptx::mma_commit(&bars.s_full[gs & 1]);
+            ++gs;
+            progress = true;
+          }
+          if (gp < gs && ptx::mbar_test_wait(&bars.p_full[gp & 1], (gp >> 1) & 1)) {
+            ptx::tc_fence_after();
+            issue_pv(gp, gp == g_first);
+            ptx::mma_commit(&bars.o_done);
+            ptx::mma_commit(&bars.stage_empty[gp % kStages]);
+            ++gp;
+            progress = true;
+          }
+          if (progress) {
+            t0 = clock64();
+          } else if (*abort_flag) {
+            ok = false;
+            break;
+          } else if (clock64() - t0 > 1000000000LL) {
+            latch_error(p.err, kErrTimeout);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+        }
+        g = g_end;
+        ++nseg;
+      }
+    }
+  } else if (warp < 4) {
+    // -------------------------------------------------------------- stage preparation
+    const int tid = threadIdx.x - 64;  // 0..63: one page row each
+    int g = 0;
+    bool ok = true;
+    while (ok && segs.next(seq, L, lo, hi)) {
+      for (int pg = lo; pg < hi; ++pg, ++g) {
+        const int s = g % kStages;
+        unsigned char* st = sm + kOffStage + s * kStageBytes;
+        const int valid = min(kPage, L - pg * kPage);  // rows holding tokens of this sequence
+        const int page = __ldg(p.page_table + (size_t)seq * p.max_pages + pg);
+        const bool bad = page < 0 || page >= p.num_pages;
+        if (bad && tid == 0) latch_error(p.err, kErrBadPage);
+        const bool live = !bad && tid < valid;
+        float ksc = 0.f;
+        if constexpr (kFp8) ksc = live ? __ldg(p.kv_scale + (size_t)page * kPage + tid) : 0.f;
+        ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.stage_full[s], (g / kStages) & 1, abort_flag, p.err));
+        if (!ok) break;
+        if constexpr (!kFp8) {
+          if (valid < kPage) {
+            // zero rows valid..63 of all 9 chunks (16-byte granules)
+            const int nrow = kPage - valid;
+            for (int e = tid; e < nrow * 9 * 8; e += kPrepThreads) {
+              const int row = valid + e / 72, rem = e % 72, c = rem >> 3, gr = rem & 7;
+              *reinterpret_cast<uint4*>(st + c * kPageChunk + row * 128 + gr * 16) = make_uint4(0, 0, 0, 0);
             }
           }
-          ptx::fence_proxy_async();
-          ptx::mbar_arrive(&bars.stage_ready[s]);
+        } else {
+          bars.kscale[s][tid] = ksc;
+          // Widen chunk by chunk, in order: bf16 chunk c (bytes [8c, 8c+8) KB) can only overlap
+          // raw chunks 2c-9 and 2c-8 (at 36 + 4c' KB).  For c < 8 those are already consumed;
+          // for c = 8 one of them is the chunk itself, read by other threads -- so every
+          // thread reads its raw row of chunk 8 before any writes (bounded mbarrier sync).
+          const int row = tid;
+#pragma unroll 1
+          for (int c = 0; c < 9; ++c) {
+            const uint4* src = reinterpret_cast<const uint4*>(st + kRawOffset + c * kRawChunk + row * 64);
+            uint4 raw[4];
+#pragma unroll
+            for (int x = 0; x < 4; ++x) raw[x] = live ? src[x] : make_uint4(0, 0, 0, 0);
+            if (c == 8) {
+              ptx::mbar_arrive(&bars.conv_sync);
+              ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.conv_sync, g & 1, abort_flag, p.err));
+              if (!ok) break;
+            }
+            const uint8_t* bytes = reinterpret_cast<const uint8_t*>(raw);
+            unsigned char* dst = st + c * kPageChunk + row * 128;
+#pragma unroll
+            for (int gr = 0; gr < 8; ++gr) {
+              uint32_t w[4];
+#pragma unroll
+              for (int x = 0; x < 4; ++x)
+                w[x] = ptx::pack_bf16x2(e4m3_to_f32(bytes[gr * 8 + 2 * x]),
+                                        e4m3_to_f32(bytes[gr * 8 + 2 * x + 1]));
+              *reinterpret_cast<uint4*>(dst + ((gr ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+          if (!ok) break;
         }
+        ptx::fence_proxy_async();
+        ptx::mbar_arrive(&bars.stage_ready[s]);
       }
     }
   } else {
@@ -287,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = threadIdx.x - 128;  // query row == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int t_row = r / p.H;
-    int g = 0, nseg = 0;
+    int g = 0;
     bool ok = true;
     while (ok && segs.next(seq, L, lo, hi)) {
       // the previous segment's MMAs are done (its epilogue waited for the last PV), so
@@ -363,14 +401,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_after();
             const float alpha = grow ? ptx::ex2(m - mx) : 1.f;  // m = -inf gives 0
             if (grow) m_use = mx;
-            uint32_t v[32];
+            uint32_t v[2][32];
 #pragma unroll 1
-            for (int c = 0; c < 8; ++c) {
-              ptx::tmem_ld32(o_addr + c * 32, v);
+            for (int c = 0; c < 8; c += 2) {
+              ptx::tmem_ld32(o_addr + c * 32, v[0]);
+              ptx::tmem_ld32(o_addr + (c + 1) * 32, v[1]);
               ptx::tmem_ld_wait();
 #pragma unroll
-              for (int x = 0; x < 32; ++x) v[x] = __float_as_uint(__uint_as_float(v[x]) * alpha);
-              ptx::tmem_st32(o_addr + c * 32, v);
+              for (int x = 0; x < 32; ++x) {
+                v[0][x] = __float_as_uint(__uint_as_float(v[0][x]) * alpha);
+                v[1][x] = __float_as_uint(__uint_as_float(v[1][x]) * alpha);
+              }
+              ptx::tmem_st32(o_addr + c * 32, v[0]);
+              ptx::tmem_st32(o_addr + (c + 1) * 32, v[1]);
             }
             l *= alpha;
             lr *= alpha;
@@ -413,22 +456,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv = lr > 0.f ? 1.f / lr : 0.f;
       float* dst = p.part_o + (slot * TH + r) * kDl + half * 256;
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
-        uint32_t v[32];
-        ptx::tmem_ld32(o_addr + c * 32, v);
+      for (int c = 0; c < 8; c += 2) {
+        uint32_t v[2][32];
+        ptx::tmem_ld32(o_addr + c * 32, v[0]);
+        ptx::tmem_ld32(o_addr + (c + 1) * 32, v[1]);
         ptx::tmem_ld_wait();
         if (r < TH) {
 #pragma unroll
-          for (int x = 0; x < 8; ++x)
-            reinterpret_cast<float4*>(dst + c * 32)[x] =
-                make_float4(__uint_as_float(v[4 * x]) * inv, __uint_as_float(v[4 * x + 1]) * inv,
-                            __uint_as_float(v[4 * x + 2]) * inv, __uint_as_float(v[4 * x + 3]) * inv);
+          for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+            for (int x = 0; x < 8; ++x)
+              reinterpret_cast<float4*>(dst + (c + h2) * 32)[x] =
+                  make_float4(__uint_as_float(v[h2][4 * x]) * inv, __uint_as_float(v[h2][4 * x + 1]) * inv,
+                              __uint_as_float(v[h2][4 * x + 2]) * inv, __uint_as_float(v[h2][4 * x + 3]) * inv);
         }
       }
       if (half == 0 && r < TH)
         p.part_lse[slot * TH + r] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
       ptx::tc_fence_before();
-      ++nseg;
     }
   }
   ptx::tc_fence_before();
@@ -443,8 +488,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- host side
 
-cudaError_t encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* ptr,
-                              const uint64_t* dims, const uint64_t* strides, const uint32_t* box);
+cudaError_t encode_tensor_map_swz(CUtensorMap* map, CUtensorMapDataType dt, int rank,
+                                  const void* ptr, const uint64_t* dims, const uint64_t* strides,
+                                  const uint32_t* box, bool swizzle128);
 
 cudaError_t launch_decode_sm103(const void* q_latent, const void* q_rope, const void* kv_cache,
                                 const float* kv_scale, const int* page_table,
@@ -454,19 +500,17 @@ cudaError_t launch_decode_sm103(const void* q_latent, const void* q_rope, const 
                                 cudaStream_t stream) {
   using namespace sm103_decode;
   CUtensorMap tm;
-  memset(&tm, 0, sizeof(tm));
-  if (!fp8) {
-    uint64_t dims[2] = {(uint64_t)kDc, (uint64_t)num_pages * kPage};
-    uint64_t strides[1] = {(uint64_t)kDc * 2};
-    uint32_t box[2] = {64, kPage};
-    cudaError_t e = encode_tensor_map(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_cache, dims,
-                                      strides, box);
-    if (e != cudaSuccess) return e;
-  }
+  // the cache as a 2-D tensor [num_pages * 64 rows, 576 columns]; boxes of 64 x 64
+  uint64_t dims[2] = {(uint64_t)kDc, (uint64_t)num_pages * kPage};
+  uint64_t strides[1] = {(uint64_t)kDc * (fp8 ? 1 : 2)};
+  uint32_t box[2] = {64, kPage};
+  cudaError_t e = encode_tensor_map_swz(
+      &tm, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_cache,
+      dims, strides, box, /*swizzle128=*/!fp8);
+  if (e != cudaSuccess) return e;
   Params p;
   p.q_latent = static_cast<const uint16_t*>(q_latent);
   p.q_rope = static_cast<const uint16_t*>(q_rope);
-  p.cache8 = static_cast<const uint8_t*>(kv_cache);
   p.kv_scale = kv_scale;
   p.page_table = page_table;
   p.cache_lens = cache_lens;
@@ -484,8 +528,8 @@ cudaError_t launch_decode_sm103(const void* q_latent, const void* q_rope, const 
   auto go = [&](auto kern) -> cudaError_t {
     static bool checked[2] = {false, false};
     if (!checked[fp8 ? 1 : 0]) {
-      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
-      if (e != cudaSuccess) return e;
+      cudaError_t e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+      if (e2 != cudaSuccess) return e2;
       checked[fp8 ? 1 : 0] = true;
     }
     kern<<<2 * G, kThreads, kSmemAlloc, stream>>>(tm, p);
