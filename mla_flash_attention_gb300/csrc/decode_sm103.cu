@@ -286,22 +286,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else {
           bars.kscale[s][tid] = ksc;
-          // Widen chunk by chunk, in order: bf16 chunk c (bytes [8c, 8c+8) KB) can only overlap
-          // raw chunks 2c-9 and 2c-8 (at 36 + 4c' KB).  For c < 8 those are already consumed;
-          // for c = 8 one of them is the chunk itself, read by other threads -- so every
-          // thread reads its raw row of chunk 8 before any writes (bounded mbarrier sync).
+          // Widen in place.  bf16 chunk c (bytes [8c, 8c+8) KB) overlaps raw chunks 2c-9 and
+          // 2c-8 (raw chunk c' sits at [36 + 4c', 40 + 4c') KB), so chunks 0..3 land below the
+          // raw bytes and can be written at once, while chunks 4..8 overwrite raw bytes other
+          // threads may still be reading: every thread first holds its raw rows of chunks
+          // 4..8 in registers, then all 64 threads meet (bounded mbarrier), then write.
           const int row = tid;
-#pragma unroll 1
-          for (int c = 0; c < 9; ++c) {
-            const uint4* src = reinterpret_cast<const uint4*>(st + kRawOffset + c * kRawChunk + row * 64);
-            uint4 raw[4];
-#pragma unroll
-            for (int x = 0; x < 4; ++x) raw[x] = live ? src[x] : make_uint4(0, 0, 0, 0);
-            if (c == 8) {
-              ptx::mbar_arrive(&bars.conv_sync);
-              ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.conv_sync, g & 1, abort_flag, p.err));
-              if (!ok) break;
-            }
+          auto widen = [&](const uint4 (&raw)[4], int c) {
             const uint8_t* bytes = reinterpret_cast<const uint8_t*>(raw);
             unsigned char* dst = st + c * kPageChunk + row * 128;
 #pragma unroll
@@ -313,8 +304,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         e4m3_to_f32(bytes[gr * 8 + 2 * x + 1]));
               *reinterpret_cast<uint4*>(dst + ((gr ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
+          };
+          auto load_raw = [&](uint4 (&raw)[4], int c) {
+            const uint4* src = reinterpret_cast<const uint4*>(st + kRawOffset + c * kRawChunk + row * 64);
+#pragma unroll
+            for (int x = 0; x < 4; ++x) raw[x] = live ? src[x] : make_uint4(0, 0, 0, 0);
+          };
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint4 raw[4];
+            load_raw(raw, c);
+            widen(raw, c);
           }
+          uint4 hold[5][4];
+#pragma unroll
+          for (int c = 4; c < 9; ++c) load_raw(hold[c - 4], c);
+          ptx::mbar_arrive(&bars.conv_sync);
+          ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.conv_sync, g & 1, abort_flag, p.err));
           if (!ok) break;
+#pragma unroll
+          for (int c = 4; c < 9; ++c) widen(hold[c - 4], c);
         }
         ptx::fence_proxy_async();
         ptx::mbar_arrive(&bars.stage_ready[s]);
