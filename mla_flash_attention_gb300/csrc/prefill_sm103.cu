@@ -48,7 +48,7 @@ struct Bars {
   uint64_t q_full;
   uint64_t ring_full[kRingSlots], ring_empty[kRingSlots];
   uint64_t rope_full[kRopeSlots], rope_empty[kRopeSlots];
-  uint64_t s_full[NQ], p_full[NQ], o_done[NQ];
+  uint64_t s_full[NQ], p_full[NQ][2], o_done[NQ];  // p_full[t][h]: keys 64h..64h+63 of P_t
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -93,7 +93,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < NQ; ++t) {
       ptx::mbar_init(&bars.s_full[t], 1);
-      ptx::mbar_init(&bars.p_full[t], BM);
+      ptx::mbar_init(&bars.p_full[t][0], BM);
+      ptx::mbar_init(&bars.p_full[t][1], BM);
       ptx::mbar_init(&bars.o_done[t], 1);
     }
     ptx::fence_barrier_init();
@@ -177,15 +178,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                ptx::mbar_wait(&bars.rope_full[j % kRopeSlots], (j / kRopeSlots) & 1, abort_flag, p.err);
       };
       // O_t (+)= P_t V(j): P_t (bf16, 64 TMEM columns over S_t), 8 k-steps of 16 keys
-      auto issue_pv = [&](int t, int j) {
+      // PV in two halves of 64 keys, each issued as soon as that half of P is in TMEM
+      auto issue_pv = [&](int t, int j) -> bool {
         const int vs = (2 * j + 1) % kRingSlots;
         const uint32_t vb = ring_base + vs * 2 * kChunk;
         const uint32_t d = tmem + 2 * BN + t * 128;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint64_t db = ptx::sw128_desc(vb + k * 2048, kChunk, 1024);
-          ptx::mma_bf16_ts(d, tmem + t * BN + k * 8, db, kIdPV, (j > 0 || k > 0) ? 1u : 0u);
+        for (int hf = 0; hf < 2; ++hf) {
+          if (!ptx::mbar_wait(&bars.p_full[t][hf], j & 1, abort_flag, p.err)) return false;
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int k = 4 * hf; k < 4 * hf + 4; ++k) {
+            const uint64_t db = ptx::sw128_desc(vb + k * 2048, kChunk, 1024);
+            ptx::mma_bf16_ts(d, tmem + t * BN + k * 8, db, kIdPV, (j > 0 || k > 0) ? 1u : 0u);
+          }
         }
+        return true;
       };
       if (ok && n_kv > 0 && (ok = wait_k(0))) {
         issue_s(0, 0);
@@ -201,9 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool more = j + 1 < n_kv;
         bool k_ready = false;
         if (j < n_kv0) {
-          if (!(ok = ptx::mbar_wait(&bars.p_full[0], j & 1, abort_flag, p.err))) break;
-          ptx::tc_fence_after();
-          issue_pv(0, j);
+          if (!(ok = issue_pv(0, j))) break;
           ptx::mma_commit(&bars.o_done[0]);
           if (j + 1 < n_kv0) {
             if (!(ok = wait_k(j + 1))) break;
@@ -212,9 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mma_commit(&bars.s_full[0]);
           }
         }
-        if (!(ok = ptx::mbar_wait(&bars.p_full[1], j & 1, abort_flag, p.err))) break;
-        ptx::tc_fence_after();
-        issue_pv(1, j);
+        if (!(ok = issue_pv(1, j))) break;
         ptx::mma_commit(&bars.o_done[1]);
         ptx::mma_commit(&bars.ring_empty[vseq % kRingSlots]);
         if (more) {
@@ -306,8 +310,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < 2; ++c) {
 #pragma unroll
         for (int x = 0; x < 32; ++x) {
-          const float p0 = ptx::ex2(fmaf(s[c * 64 + 2 * x], p.scale_log2, neg_m));
-          const float p1 = ptx::ex2(fmaf(s[c * 64 + 2 * x + 1], p.scale_log2, neg_m));
+          // one exponential in four on the FMA pipe (polynomial), the rest on the SFU
+          const float a0 = fmaf(s[c * 64 + 2 * x], p.scale_log2, neg_m);
+          const float a1 = fmaf(s[c * 64 + 2 * x + 1], p.scale_log2, neg_m);
+          const float p0 = ptx::ex2(a0);
+          const float p1 = (x & 1) ? ptx::ex2_poly(a1) : ptx::ex2(a1);
           // O is normalised by the sum of the bf16-rounded values the PV product uses (so a
           // dominant key is normalised exactly); the LSE uses the exact sum
           const uint32_t w = ptx::pack_bf16x2(p0, p1);
@@ -316,12 +323,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           pr[x & 3] += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
         }
         ptx::tmem_st32(s_addr + c * 32, pk);
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&bars.p_full[t][c]);
       }
       l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
       lr += (pr[0] + pr[1]) + (pr[2] + pr[3]);
-      ptx::tmem_st_wait();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&bars.p_full[t]);
     }
     // epilogue: O / l -> out, LSE
     if (ok && n_t > 0 &&
