@@ -153,8 +153,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&bars.s_full[i], 1);
       ptx::mbar_init(&bars.p_full[i], kRows);
-      ptx::mbar_init(&bars.recv_full[i], kRows);
-      ptx::mbar_init(&bars.send_ok[i], kRows);
+      ptx::mbar_init(&bars.recv_full[i], kRows / 32);  // one arrival per softmax warp
+      ptx::mbar_init(&bars.send_ok[i], kRows / 32);
     }
     ptx::mbar_init(&bars.o_done, 1);
     ptx::mbar_init(&bars.q_ready, kRows);
@@ -358,6 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // -------------------------------------------------------------- softmax / Q / epilogue
     const int r = threadIdx.x - 128;  // query row == TMEM lane
+    const int lane = threadIdx.x & 31;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int t_row = r / p.H;
     // this row of the other rank's receive buffers, and its barriers
@@ -416,18 +417,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(own + 32));
           ptx::tmem_ld_wait();
           // send the own partial scores to the other rank (its buffer xb is free once it has
-          // read what it got two pages ago)
+          // read what it got two pages ago).  One lane per warp waits / arrives for the warp:
+          // __syncwarp orders the other lanes' shared-memory traffic around it.
           if (g >= 2) {
-            ok = __all_sync(0xffffffffu, ptx::mbar_wait_cluster(&bars.send_ok[xb], ((g >> 1) - 1) & 1, abort_flag, p.err));
+            bool w = true;
+            if (lane == 0) w = ptx::mbar_wait_cluster(&bars.send_ok[xb], ((g >> 1) - 1) & 1, abort_flag, p.err);
+            ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
             if (!ok) break;
           }
 #pragma unroll
           for (int x = 0; x < 16; ++x)
             ptx::st_cluster_v4(xrow_peer + xb * kXBuf + x * 16, own[4 * x], own[4 * x + 1], own[4 * x + 2], own[4 * x + 3]);
-          ptx::mbar_arrive_remote(peer_recv_full[xb]);
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive_remote(peer_recv_full[xb]);
           // receive the other rank's partial scores and add them in rank order
-          ok = __all_sync(0xffffffffu, ptx::mbar_wait_cluster(&bars.recv_full[xb], (g >> 1) & 1, abort_flag, p.err));
-          if (!ok) break;
+          {
+            bool w = true;
+            if (lane == 0) w = ptx::mbar_wait_cluster(&bars.recv_full[xb], (g >> 1) & 1, abort_flag, p.err);
+            ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+            if (!ok) break;
+          }
           const float4* in = reinterpret_cast<const float4*>(sm + kOffXchg + xb * kXBuf + r * kXRow);
 #pragma unroll
           for (int x = 0; x < 16; ++x) {
@@ -440,7 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               s[4 * x] = o.x + a0; s[4 * x + 1] = o.y + a1; s[4 * x + 2] = o.z + a2; s[4 * x + 3] = o.w + a3;
             }
           }
-          ptx::mbar_arrive_remote(peer_send_ok[xb]);
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive_remote(peer_send_ok[xb]);
         }
         const int page = __ldg(p.page_table + (size_t)seq * p.max_pages + pg);
         const bool bad = page < 0 || page >= p.num_pages;
