@@ -41,8 +41,9 @@ constexpr int kMaxOwn = 5;                          // rank 0: 4 latent chunks +
 constexpr int kStageBytes = kMaxOwn * kPageChunk;   // 40 KB
 constexpr int kRawChunk = kPage * 64;               // 64 rows x 64 fp8 bytes (4 KB), unswizzled
 constexpr int kStages = 3;
-constexpr int kXRow = 64 * 4 + 16;                  // one row of partial scores, padded
-constexpr int kXBuf = kRows * kXRow;                // 34 KB
+// Partial scores of one page, stored as [16 groups of 4 keys][128 rows] of float4 so the
+// 32 lanes of a warp (consecutive rows) read and write 512 contiguous bytes at a time.
+constexpr int kXBuf = kRows * 64 * 4;               // 32 KB
 constexpr int kOffQrope = 0;                        // rank 0: rope part of Q (16 KB)
 constexpr int kOffXchg = 16 * 1024;                 // two receive buffers of partial scores
 constexpr int kOffStage = kOffXchg + 2 * kXBuf;     // 84 KB (1024-aligned)
@@ -362,8 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int t_row = r / p.H;
     // this row of the other rank's receive buffers, and its barriers
-    const uint32_t xrow_local = ptx::smem_u32(sm + kOffXchg + r * kXRow);
-    const uint32_t xrow_peer = ptx::map_to_rank(xrow_local, peer);
+    const uint32_t xrow_peer = ptx::map_to_rank(ptx::smem_u32(sm + kOffXchg + r * 16), peer);
     const uint32_t peer_recv_full[2] = {ptx::map_to_rank(ptx::smem_u32(&bars.recv_full[0]), peer),
                                         ptx::map_to_rank(ptx::smem_u32(&bars.recv_full[1]), peer)};
     const uint32_t peer_send_ok[2] = {ptx::map_to_rank(ptx::smem_u32(&bars.send_ok[0]), peer),
@@ -427,7 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int x = 0; x < 16; ++x)
-            ptx::st_cluster_v4(xrow_peer + xb * kXBuf + x * 16, own[4 * x], own[4 * x + 1], own[4 * x + 2], own[4 * x + 3]);
+            ptx::st_cluster_v4(xrow_peer + xb * kXBuf + x * (kRows * 16), own[4 * x], own[4 * x + 1],
+                               own[4 * x + 2], own[4 * x + 3]);
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive_remote(peer_recv_full[xb]);
           // receive the other rank's partial scores and add them in rank order
@@ -437,10 +438,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
             if (!ok) break;
           }
-          const float4* in = reinterpret_cast<const float4*>(sm + kOffXchg + xb * kXBuf + r * kXRow);
+          const float4* in = reinterpret_cast<const float4*>(sm + kOffXchg + xb * kXBuf) + r;
 #pragma unroll
           for (int x = 0; x < 16; ++x) {
-            const float4 o = in[x];
+            const float4 o = in[x * kRows];
             const float a0 = __uint_as_float(own[4 * x]), a1 = __uint_as_float(own[4 * x + 1]);
             const float a2 = __uint_as_float(own[4 * x + 2]), a3 = __uint_as_float(own[4 * x + 3]);
             if (rank == 0) {
