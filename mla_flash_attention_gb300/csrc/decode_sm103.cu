@@ -1,30 +1,25 @@
 // Absorbed MLA decode over the paged latent cache on tcgen05 / TMEM (split-KV part).
 //
-// Each work unit (a contiguous range of pages from the split plan) is served by a cluster
-// of two CTAs that split the 576-wide latent+rope axis between them: rank 0 owns latent
-// columns 0..255 and the 64 rope columns, rank 1 owns latent columns 256..511.  Per page,
-// each rank computes the partial scores of its own columns (S_r = Q[:, own] C[:, own]'),
-// the two fp32 partials are exchanged through distributed shared memory and added in the
-// same order on both sides (so both hold bitwise identical scores and probabilities), and
-// each rank accumulates the half of O = P C[:, latent] that its own columns give.  Nothing
-// is computed twice and each rank loads only its own columns of the cache.  O for 128
-// query rows x 256 columns fills half of the TMEM; query rows are the (token, head) pairs
+// Each work unit (a contiguous range of pages from the split plan) is served by a pair
+// of CTAs that differ only in which half of the 512 latent output columns they own:
+// O (128 query rows x 512 fp32) is exactly the 512-column TMEM, so one CTA cannot also
+// hold the scores.  Both CTAs of a pair compute the full scores S = Q C' (the redundant
+// part) and their own half of O += P C[:, half].  Query rows are the (token, head) pairs
 // of one sequence, padded to the MMA's M = 128.
 //
 // Per CTA (8 warps):
-//   warp 0      TMA producer: this rank's chunks (64 keys x 64 columns each) of one cache
-//               page per stage -- bf16: 128B-swizzled, ready for the MMA; fp8: raw bytes into
-//               the upper half of the stage -- plus L2 prefetch of pages ahead
-//   warp 1      MMA issuer: S_r(g) = Q C(g)' over the own columns into one of two S
-//               buffers (A = Q latent part from TMEM, rope part from shared memory), then
-//               O_half += P(g) C(g)[:, own latent] with P read from TMEM.  S(g+1) and PV(g)
-//               are issued in whichever order their inputs arrive.
+//   warp 0      TMA producer: one cache page (64 keys x 576 columns) per stage, as nine
+//               64-column chunks -- bf16: 128B-swizzled, ready for the MMA; fp8: raw bytes
+//               into the upper half of the stage -- plus L2 prefetch of pages ahead
+//   warp 1      MMA issuer: S(g) = Q C(g)' into one of two S buffers (A operand = Q:
+//               latent 0..255 from TMEM, latent 256..511 + rope from shared memory), then
+//               O_half += P(g) C(g)[:, half] with P read from TMEM.  S(g+1) and PV(g) are
+//               issued in whichever order their inputs arrive.
 //   warps 2-3   stage preparation: zero the rows past the sequence end of a partial page;
-//               fp8: widen the own chunks to bf16 in place and stage the row scales
-//   warps 4-7   softmax, one thread per query row: exchange of the partial scores with the
-//               other rank, online softmax, P (bf16) into TMEM; they also load each
-//               sequence's Q and write the split's partial (O_half / l, log-sum-exp)
-// TMEM columns: [0,128) Q own latent (bf16 pairs), [128,256) two S / P buffers of 64,
+//               fp8: widen the page to bf16 in place (chunk by chunk) and stage its scales
+//   warps 4-7   softmax, one thread per query row; they also load each sequence's Q and
+//               write the split's partial (O_half / l, log-sum-exp)
+// TMEM columns: [0,128) Q latent 0..255 (bf16 pairs), [128,256) two S / P buffers of 64,
 // [256,512) O half.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -36,24 +31,19 @@ namespace mla {
 namespace sm103_decode {
 
 constexpr int kPage = 64, kDl = 512, kDc = 576, kRows = 128;
-constexpr int kPageChunk = kPage * 128;             // 64 rows x 64 bf16 (8 KB), 128B-swizzled
-constexpr int kMaxOwn = 5;                          // rank 0: 4 latent chunks + rope; rank 1: 4
-constexpr int kStageBytes = kMaxOwn * kPageChunk;   // 40 KB
-constexpr int kRawChunk = kPage * 64;               // 64 rows x 64 fp8 bytes (4 KB), unswizzled
-constexpr int kStages = 3;
-// Partial scores of one page, stored as [16 groups of 4 keys][128 rows] of float4 so the
-// 32 lanes of a warp (consecutive rows) read and write 512 contiguous bytes at a time.
-constexpr int kXBuf = kRows * 64 * 4;               // 32 KB
-constexpr int kOffQrope = 0;                        // rank 0: rope part of Q (16 KB)
-constexpr int kOffXchg = 16 * 1024;                 // two receive buffers of partial scores
-constexpr int kOffStage = kOffXchg + 2 * kXBuf;     // 84 KB (1024-aligned)
-constexpr int kSmemBytes = kOffStage + kStages * kStageBytes;  // 204 KB
+constexpr int kPageChunk = kPage * 128;       // 64 rows x 64 bf16 (8 KB), 128B-swizzled
+constexpr int kStageBytes = 9 * kPageChunk;   // 72 KB
+constexpr int kRawChunk = kPage * 64;         // 64 rows x 64 fp8 bytes (4 KB), unswizzled
+constexpr int kRawOffset = 9 * kRawChunk;     // fp8 page lands in the upper 36 KB of a stage
+constexpr int kStages = 2;
+constexpr int kQChunk = kRows * 128;          // 128 rows x 64 bf16 (16 KB)
+constexpr int kOffQhi = 0;                    // latent 256..511 (4 chunks) + rope (1 chunk)
+constexpr int kOffStage = 5 * kQChunk;        // 80 KB
+constexpr int kSmemBytes = kOffStage + kStages * kStageBytes;  // 224 KB
 constexpr int kSmemAlloc = kSmemBytes + 1024;
 constexpr int kThreads = 256;
 constexpr int kPrepThreads = 64;
-constexpr int kPrefetchAhead = 4;                   // pages warmed in L2 ahead of their load
-
-static_assert(kOffStage % 1024 == 0, "stages must be 1024-byte aligned");
+constexpr int kPrefetchAhead = 4;             // pages warmed in L2 ahead of their load
 
 struct Params {
   const uint16_t* q_latent;  // [B, T, H, 512]
@@ -71,7 +61,6 @@ struct Params {
 struct Bars {
   uint64_t stage_full[kStages], stage_ready[kStages], stage_empty[kStages];
   uint64_t s_full[2], p_full[2], o_done, q_ready, conv_sync;
-  uint64_t recv_full[2], send_ok[2];  // arrived by the other rank
   uint32_t tmem_base;
   int abort_flag;
   float kscale[kStages][kPage];
@@ -125,11 +114,6 @@ __device__ __forceinline__ int page_row(const Params& p, int seq, int pg) {
   return (page >= 0 && page < p.num_pages) ? page * kPage : -2 * kPage;
 }
 
-// Global 64-column chunk index of this rank's k-th chunk (rank 0: 0,1,2,3 and rope 8).
-__device__ __forceinline__ int own_chunk(int rank, int k) {
-  return rank == 0 ? (k < 4 ? k : 8) : 4 + k;
-}
-
 template <bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_cache, const Params p) {
@@ -138,10 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   __shared__ Bars bars;
   const int warp = threadIdx.x >> 5;
-  const int unit = blockIdx.x >> 1;
-  const int rank = static_cast<int>(ptx::cluster_ctarank());
-  const int peer = rank ^ 1;
-  const int nown = rank == 0 ? 5 : 4;  // own chunks per page
+  const int unit = blockIdx.x >> 1, half = blockIdx.x & 1;
   const int TH = p.T * p.H;
 
   if (threadIdx.x == 0) {
@@ -154,8 +135,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&bars.s_full[i], 1);
       ptx::mbar_init(&bars.p_full[i], kRows);
-      ptx::mbar_init(&bars.recv_full[i], kRows / 32);  // one arrival per softmax warp
-      ptx::mbar_init(&bars.send_ok[i], kRows / 32);
     }
     ptx::mbar_init(&bars.o_done, 1);
     ptx::mbar_init(&bars.q_ready, kRows);
@@ -165,7 +144,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 2) ptx::tmem_alloc(&bars.tmem_base, 512);
   ptx::tc_fence_before();
   __syncthreads();
-  ptx::cluster_sync();  // both ranks' barriers exist before any remote arrive
   ptx::tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
   volatile int* abort_flag = &bars.abort_flag;
@@ -180,26 +158,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       int g = 0;
       bool ok = true;
       const int chunk_bytes = kFp8 ? kRawChunk : kPageChunk;
-      const int raw_off = kFp8 ? nown * kRawChunk : 0;  // fp8 bytes sit in the upper half
       while (ok && segs.next(seq, L, lo, hi)) {
         for (int a = lo; a < min(hi, lo + kPrefetchAhead); ++a) {
           const int y = page_row(p, seq, a);
           if (y >= 0)
-            for (int k = 0; k < nown; ++k) ptx::tma_prefetch_2d(&tm_cache, own_chunk(rank, k) * 64, y);
+            for (int c = 0; c < 9; ++c) ptx::tma_prefetch_2d(&tm_cache, c * 64, y);
         }
         for (int pg = lo; pg < hi; ++pg, ++g) {
           if (pg + kPrefetchAhead < hi) {
             const int ya = page_row(p, seq, pg + kPrefetchAhead);
             if (ya >= 0)
-              for (int k = 0; k < nown; ++k) ptx::tma_prefetch_2d(&tm_cache, own_chunk(rank, k) * 64, ya);
+              for (int c = 0; c < 9; ++c) ptx::tma_prefetch_2d(&tm_cache, c * 64, ya);
           }
           const int s = g % kStages;
           if (!(ok = ptx::mbar_wait(&bars.stage_empty[s], ((g / kStages) & 1) ^ 1, abort_flag, p.err))) break;
           const int y = page_row(p, seq, pg);
-          unsigned char* dst = sm + kOffStage + s * kStageBytes + raw_off;
-          ptx::mbar_arrive_expect_tx(&bars.stage_full[s], nown * chunk_bytes);
-          for (int k = 0; k < nown; ++k)
-            ptx::tma_load_2d(dst + k * chunk_bytes, &tm_cache, &bars.stage_full[s], own_chunk(rank, k) * 64, y);
+          unsigned char* dst = sm + kOffStage + s * kStageBytes + (kFp8 ? kRawOffset : 0);
+          ptx::mbar_arrive_expect_tx(&bars.stage_full[s], 9 * chunk_bytes);
+          for (int c = 0; c < 9; ++c)
+            ptx::tma_load_2d(dst + c * chunk_bytes, &tm_cache, &bars.stage_full[s], c * 64, y);
         }
       }
     }
@@ -208,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ptx::elect_one()) {
       constexpr uint32_t kIdS = ptx::make_idesc(1, kRows, kPage, 0, 0);
       constexpr uint32_t kIdPV = ptx::make_idesc(1, kRows, 256, 0, 1);
-      const uint32_t qrope = ptx::smem_u32(sm + kOffQrope);
+      const uint32_t qhi = ptx::smem_u32(sm + kOffQhi);
       const uint32_t stage0 = ptx::smem_u32(sm + kOffStage);
       const uint32_t o_tm = tmem + 256;
       int g = 0, nseg = 0;
@@ -217,21 +194,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t st = stage0 + (gg % kStages) * kStageBytes;
         const uint32_t d = tmem + 128 + (gg & 1) * 64;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {  // own latent columns: A from TMEM
+        for (int k = 0; k < 16; ++k) {  // latent 0..255: A from TMEM
           const uint64_t db = ptx::sw128_desc(st + (k >> 2) * kPageChunk + (k & 3) * 32, 16, 1024);
           ptx::mma_bf16_ts(d, tmem + k * 8, db, kIdS, k > 0);
         }
-        if (rank == 0) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {  // rope columns: A from shared memory
-            const uint64_t da = ptx::sw128_desc(qrope + k * 32, 16, 1024);
-            const uint64_t db = ptx::sw128_desc(st + 4 * kPageChunk + k * 32, 16, 1024);
-            ptx::mma_bf16_ss(d, da, db, kIdS, 1);
-          }
+        for (int k = 16; k < 36; ++k) {  // latent 256..511 + rope: A from shared memory
+          const int kq = k - 16;
+          const uint64_t da = ptx::sw128_desc(qhi + (kq >> 2) * kQChunk + (kq & 3) * 32, 16, 1024);
+          const uint64_t db = ptx::sw128_desc(st + (k >> 2) * kPageChunk + (k & 3) * 32, 16, 1024);
+          ptx::mma_bf16_ss(d, da, db, kIdS, 1);
         }
       };
       auto issue_pv = [&](int gg, bool first) {
-        const uint32_t st = stage0 + (gg % kStages) * kStageBytes;
+        const uint32_t st = stage0 + (gg % kStages) * kStageBytes + 4 * half * kPageChunk;
         const uint32_t pa = tmem + 128 + (gg & 1) * 64;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -301,25 +277,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         if constexpr (!kFp8) {
           if (valid < kPage) {
-            // zero rows valid..63 of the own chunks (16-byte granules)
-            const int nrow = kPage - valid, per_row = nown * 8;
-            for (int e = tid; e < nrow * per_row; e += kPrepThreads) {
-              const int row = valid + e / per_row, rem = e % per_row, c = rem >> 3, gr = rem & 7;
+            // zero rows valid..63 of all 9 chunks (16-byte granules)
+            const int nrow = kPage - valid;
+            for (int e = tid; e < nrow * 9 * 8; e += kPrepThreads) {
+              const int row = valid + e / 72, rem = e % 72, c = rem >> 3, gr = rem & 7;
               *reinterpret_cast<uint4*>(st + c * kPageChunk + row * 128 + gr * 16) = make_uint4(0, 0, 0, 0);
             }
           }
         } else {
           bars.kscale[s][tid] = ksc;
-          // Widen in place.  With R = nown * 4 KB, raw chunk k sits at [R + 4k, R + 4k + 4) KB and
-          // bf16 chunk k at [8k, 8k + 8) KB: chunks 0 and 1 land below every raw byte, chunks
-          // 2.. overwrite raw bytes other threads may still be reading -- every thread holds
-          // its raw rows of chunks 2.. in registers, all 64 threads meet (bounded mbarrier),
-          // then those are written.
+          // Widen in place.  bf16 chunk c (bytes [8c, 8c+8) KB) overlaps raw chunks 2c-9 and
+          // 2c-8 (raw chunk c' sits at [36 + 4c', 40 + 4c') KB), so chunks 0..3 land below the
+          // raw bytes and can be written at once, while chunks 4..8 overwrite raw bytes other
+          // threads may still be reading: every thread first holds its raw rows of chunks
+          // 4..8 in registers, then all 64 threads meet (bounded mbarrier), then write.
           const int row = tid;
-          const unsigned char* raw_base = st + nown * kRawChunk;
-          auto widen = [&](const uint4 (&raw)[4], int k) {
+          auto widen = [&](const uint4 (&raw)[4], int c) {
             const uint8_t* bytes = reinterpret_cast<const uint8_t*>(raw);
-            unsigned char* dst = st + k * kPageChunk + row * 128;
+            unsigned char* dst = st + c * kPageChunk + row * 128;
 #pragma unroll
             for (int gr = 0; gr < 8; ++gr) {
               uint32_t w[4];
@@ -330,27 +305,25 @@ __global__ void __launch_bounds__(kThreads, 1)
               *reinterpret_cast<uint4*>(dst + ((gr ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
           };
-          auto load_raw = [&](uint4 (&raw)[4], int k) {
-            const uint4* src = reinterpret_cast<const uint4*>(raw_base + k * kRawChunk + row * 64);
+          auto load_raw = [&](uint4 (&raw)[4], int c) {
+            const uint4* src = reinterpret_cast<const uint4*>(st + kRawOffset + c * kRawChunk + row * 64);
 #pragma unroll
             for (int x = 0; x < 4; ++x) raw[x] = live ? src[x] : make_uint4(0, 0, 0, 0);
           };
 #pragma unroll 1
-          for (int k = 0; k < 2; ++k) {
+          for (int c = 0; c < 4; ++c) {
             uint4 raw[4];
-            load_raw(raw, k);
-            widen(raw, k);
+            load_raw(raw, c);
+            widen(raw, c);
           }
-          uint4 hold[3][4];
+          uint4 hold[5][4];
 #pragma unroll
-          for (int k = 2; k < kMaxOwn; ++k)
-            if (k < nown) load_raw(hold[k - 2], k);
+          for (int c = 4; c < 9; ++c) load_raw(hold[c - 4], c);
           ptx::mbar_arrive(&bars.conv_sync);
           ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.conv_sync, g & 1, abort_flag, p.err));
           if (!ok) break;
 #pragma unroll
-          for (int k = 2; k < kMaxOwn; ++k)
-            if (k < nown) widen(hold[k - 2], k);
+          for (int c = 4; c < 9; ++c) widen(hold[c - 4], c);
         }
         ptx::fence_proxy_async();
         ptx::mbar_arrive(&bars.stage_ready[s]);
@@ -359,41 +332,44 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // -------------------------------------------------------------- softmax / Q / epilogue
     const int r = threadIdx.x - 128;  // query row == TMEM lane
-    const int lane = threadIdx.x & 31;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int t_row = r / p.H;
-    // this row of the other rank's receive buffers, and its barriers
-    const uint32_t xrow_peer = ptx::map_to_rank(ptx::smem_u32(sm + kOffXchg + r * 16), peer);
-    const uint32_t peer_recv_full[2] = {ptx::map_to_rank(ptx::smem_u32(&bars.recv_full[0]), peer),
-                                        ptx::map_to_rank(ptx::smem_u32(&bars.recv_full[1]), peer)};
-    const uint32_t peer_send_ok[2] = {ptx::map_to_rank(ptx::smem_u32(&bars.send_ok[0]), peer),
-                                      ptx::map_to_rank(ptx::smem_u32(&bars.send_ok[1]), peer)};
     int g = 0;
     bool ok = true;
     while (ok && segs.next(seq, L, lo, hi)) {
       // the previous segment's MMAs are done (its epilogue waited for the last PV), so
-      // Q can be overwritten: own latent columns -> TMEM, rope (rank 0) -> smem
+      // Q can be overwritten: latent 0..255 -> TMEM columns 0..127, the rest -> smem
       {
         const bool live = r < TH;
         const size_t qrow = (size_t)seq * TH + r;
-        const uint4* ql = reinterpret_cast<const uint4*>(p.q_latent + qrow * kDl) + rank * 32;
-        uint32_t v[4][32];
+        const uint4* ql = reinterpret_cast<const uint4*>(p.q_latent + qrow * kDl);
+        const uint4* qr = reinterpret_cast<const uint4*>(p.q_rope + qrow * 64);
+        {  // latent 0..255: all 32 loads in flight, then 4 x 32 TMEM columns
+          uint32_t v[4][32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int x = 0; x < 8; ++x) {
-            const uint4 u = live ? __ldg(ql + c * 8 + x) : make_uint4(0, 0, 0, 0);
-            v[c][4 * x] = u.x; v[c][4 * x + 1] = u.y; v[c][4 * x + 2] = u.z; v[c][4 * x + 3] = u.w;
-          }
+            for (int x = 0; x < 8; ++x) {
+              const uint4 u = live ? __ldg(ql + c * 8 + x) : make_uint4(0, 0, 0, 0);
+              v[c][4 * x] = u.x; v[c][4 * x + 1] = u.y; v[c][4 * x + 2] = u.z; v[c][4 * x + 3] = u.w;
+            }
 #pragma unroll
-        for (int c = 0; c < 4; ++c) ptx::tmem_st32(tmem + lane_off + c * 32, v[c]);
-        if (rank == 0) {
-          const uint4* qr = reinterpret_cast<const uint4*>(p.q_rope + qrow * 64);
-          unsigned char* dst = sm + kOffQrope + r * 128;
+          for (int c = 0; c < 4; ++c) ptx::tmem_st32(tmem + lane_off + c * 32, v[c]);
+        }
 #pragma unroll
-          for (int x = 0; x < 8; ++x) {
-            const uint4 u = live ? __ldg(qr + x) : make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(dst + ((x ^ (r & 7)) << 4)) = u;
+        for (int half_q = 0; half_q < 2; ++half_q) {  // latent 256..511 (4 chunks) + rope
+          const int c0 = half_q * 2, c1 = half_q ? 5 : 2;
+          uint4 u[3][8];
+#pragma unroll
+          for (int c = c0; c < c1; ++c)
+#pragma unroll
+            for (int x = 0; x < 8; ++x)
+              u[c - c0][x] = !live ? make_uint4(0, 0, 0, 0) : (c < 4 ? __ldg(ql + 32 + c * 8 + x) : __ldg(qr + x));
+#pragma unroll
+          for (int c = c0; c < c1; ++c) {
+            unsigned char* dst = sm + kOffQhi + c * kQChunk + r * 128;
+#pragma unroll
+            for (int x = 0; x < 8; ++x) *reinterpret_cast<uint4*>(dst + ((x ^ (r & 7)) << 4)) = u[c - c0][x];
           }
         }
         ptx::tmem_st_wait();
@@ -409,49 +385,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         ptx::tc_fence_after();
         const uint32_t s_addr = tmem + lane_off + 128 + (g & 1) * 64;
-        const int xb = g & 1;
         float s[64];
         {
-          uint32_t own[64];
-          ptx::tmem_ld32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(own));
-          ptx::tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(own + 32));
+          uint32_t* su = reinterpret_cast<uint32_t*>(s);
+          ptx::tmem_ld32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(su));
+          ptx::tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(su + 32));
           ptx::tmem_ld_wait();
-          // send the own partial scores to the other rank (its buffer xb is free once it has
-          // read what it got two pages ago).  One lane per warp waits / arrives for the warp:
-          // __syncwarp orders the other lanes' shared-memory traffic around it.
-          if (g >= 2) {
-            bool w = true;
-            if (lane == 0) w = ptx::mbar_wait_cluster(&bars.send_ok[xb], ((g >> 1) - 1) & 1, abort_flag, p.err);
-            ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
-            if (!ok) break;
-          }
-#pragma unroll
-          for (int x = 0; x < 16; ++x)
-            ptx::st_cluster_v4(xrow_peer + xb * kXBuf + x * (kRows * 16), own[4 * x], own[4 * x + 1],
-                               own[4 * x + 2], own[4 * x + 3]);
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive_remote(peer_recv_full[xb]);
-          // receive the other rank's partial scores and add them in rank order
-          {
-            bool w = true;
-            if (lane == 0) w = ptx::mbar_wait_cluster(&bars.recv_full[xb], (g >> 1) & 1, abort_flag, p.err);
-            ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
-            if (!ok) break;
-          }
-          const float4* in = reinterpret_cast<const float4*>(sm + kOffXchg + xb * kXBuf) + r;
-#pragma unroll
-          for (int x = 0; x < 16; ++x) {
-            const float4 o = in[x * kRows];
-            const float a0 = __uint_as_float(own[4 * x]), a1 = __uint_as_float(own[4 * x + 1]);
-            const float a2 = __uint_as_float(own[4 * x + 2]), a3 = __uint_as_float(own[4 * x + 3]);
-            if (rank == 0) {
-              s[4 * x] = a0 + o.x; s[4 * x + 1] = a1 + o.y; s[4 * x + 2] = a2 + o.z; s[4 * x + 3] = a3 + o.w;
-            } else {
-              s[4 * x] = o.x + a0; s[4 * x + 1] = o.y + a1; s[4 * x + 2] = o.z + a2; s[4 * x + 3] = o.w + a3;
-            }
-          }
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive_remote(peer_send_ok[xb]);
         }
         const int page = __ldg(p.page_table + (size_t)seq * p.max_pages + pg);
         const bool bad = page < 0 || page >= p.num_pages;
@@ -533,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_after();
       const size_t slot = (size_t)unit + seq;
       const float inv = lr > 0.f ? 1.f / lr : 0.f;
-      float* dst = p.part_o + (slot * TH + r) * kDl + rank * 256;
+      float* dst = p.part_o + (slot * TH + r) * kDl + half * 256;
 #pragma unroll 1
       for (int c = 0; c < 8; c += 2) {
         uint32_t v[2][32];
@@ -550,14 +489,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                               __uint_as_float(v[h2][4 * x + 2]) * inv, __uint_as_float(v[h2][4 * x + 3]) * inv);
         }
       }
-      if (rank == 0 && r < TH)
+      if (half == 0 && r < TH)
         p.part_lse[slot * TH + r] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
       ptx::tc_fence_before();
     }
   }
   ptx::tc_fence_before();
   __syncthreads();
-  ptx::cluster_sync();  // the other rank no longer touches this CTA's shared memory
   if (warp == 2) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 512);
@@ -612,19 +550,8 @@ cudaError_t launch_decode_sm103(const void* q_latent, const void* q_rope, const 
       if (e2 != cudaSuccess) return e2;
       checked[fp8 ? 1 : 0] = true;
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * G, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmemAlloc;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, tm, p);
+    kern<<<2 * G, kThreads, kSmemAlloc, stream>>>(tm, p);
+    return cudaGetLastError();
   };
   return fp8 ? go(decode_split_kernel<true>) : go(decode_split_kernel<false>);
 }

@@ -310,11 +310,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < 2; ++c) {
 #pragma unroll
         for (int x = 0; x < 32; ++x) {
-          // one exponential in four on the FMA pipe (polynomial), the rest on the SFU
           const float a0 = fmaf(s[c * 64 + 2 * x], p.scale_log2, neg_m);
           const float a1 = fmaf(s[c * 64 + 2 * x + 1], p.scale_log2, neg_m);
           const float p0 = ptx::ex2(a0);
-          const float p1 = (x & 1) ? ptx::ex2_poly(a1) : ptx::ex2(a1);
+          const float p1 = ptx::ex2(a1);
           // O is normalised by the sum of the bf16-rounded values the PV product uses (so a
           // dominant key is normalised exactly); the LSE uses the exact sum
           const uint32_t w = ptx::pack_bf16x2(p0, p1);
