@@ -38,25 +38,11 @@ __device__ __forceinline__ int pages_of(int L, int page_size) {
   return L > 0 ? (L + page_size - 1) / page_size : 0;
 }
 
-// Split plan of the decode key axis (computed identically by every CTA that needs
+// Split plan of the decode key axis (computed identically by every kernel that needs
 // it, from cache_lens alone): the pages of all sequences are numbered in sequence
-// order (sequence b owns flat pages [P_b, P_b + n_b)), and work CTA c of G takes flat
+// order (sequence b owns flat pages [P_b, P_b + n_b)), and work unit c of G takes flat
 // pages [c*chunk, (c+1)*chunk) with chunk = ceil(total / G).  The partial result of
-// CTA c for sequence b goes to slot c + b, which is unique because consecutive CTAs
+// unit c for sequence b goes to slot c + b, which is unique because consecutive units
 // never move backwards through the sequences; there are at most G + B - 1 slots.
-struct SplitPlan {
-  int total;  // pages over all sequences
-  int chunk;  // pages per work CTA
-};
-
-__device__ __forceinline__ SplitPlan make_split_plan(const int* cache_lens, int B,
-                                                     int page_size, int G) {
-  int total = 0;
-  for (int b = 0; b < B; ++b) total += pages_of(__ldg(cache_lens + b), page_size);
-  SplitPlan p;
-  p.total = total;
-  p.chunk = total > 0 ? (total + G - 1) / G : 1;
-  return p;
-}
 
 }  // namespace mla

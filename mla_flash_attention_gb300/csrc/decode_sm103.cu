@@ -8,17 +8,20 @@
 // of one sequence, padded to the MMA's M = 128.
 //
 // Per CTA (8 warps):
-//   warp 0      TMA producer: one cache page (64 keys x 576 columns) per stage, as nine
-//               64-column chunks -- bf16: 128B-swizzled, ready for the MMA; fp8: raw bytes
-//               into the upper half of the stage -- plus L2 prefetch of pages ahead
-//   warp 1      MMA issuer: S(g) = Q C(g)' into one of two S buffers (A operand = Q:
-//               latent 0..255 from TMEM, latent 256..511 + rope from shared memory), then
-//               O_half += P(g) C(g)[:, half] with P read from TMEM.  S(g+1) and PV(g) are
-//               issued in whichever order their inputs arrive.
+//   warp 0      TMA producer: each sequence's Q latent 0..255 (staged in shared memory),
+//               then one cache page (64 keys x 576 columns) per stage, as nine 64-column
+//               chunks -- bf16: 128B-swizzled, ready for the MMA; fp8: raw bytes into the
+//               upper half of the stage -- plus L2 prefetch of pages ahead
+//   warp 1      MMA issuer: at a sequence change, copies the staged Q latent 0..255 into
+//               TMEM (tcgen05.cp) and loads latent 256..511 + rope into shared memory by TMA;
+//               then S(g) = Q C(g)' into one of two S buffers (A operand = Q: latent 0..255
+//               from TMEM, the rest from shared memory), and O_half += P(g) C(g)[:, half]
+//               with P read from TMEM.  S(g+1) and PV(g) are issued in whichever order their
+//               inputs arrive.
 //   warps 2-3   stage preparation: zero the rows past the sequence end of a partial page;
 //               fp8: widen the page to bf16 in place (chunk by chunk) and stage its scales
-//   warps 4-7   softmax, one thread per query row; they also load each sequence's Q and
-//               write the split's partial (O_half / l, log-sum-exp)
+//   warps 4-7   softmax, one thread per query row; they also write the split's partial
+//               (O_half / l, log-sum-exp), column quads of 32 rows per 512-byte store
 // TMEM columns: [0,128) Q latent 0..255 (bf16 pairs), [128,256) two S / P buffers of 64,
 // [256,512) O half.
 #include <cuda.h>
@@ -58,11 +61,19 @@ struct Params {
   float scale_log2;
 };
 
+// The work unit's page range [start, end) of the flat page numbering and the first
+// sequence that reaches into it (b0, whose pages start at flat page pb0).
+struct Plan {
+  int start, end, b0, pb0;
+};
+
 struct Bars {
   uint64_t stage_full[kStages], stage_ready[kStages], stage_empty[kStages];
-  uint64_t s_full[2], p_full[2], o_done, q_ready, conv_sync;
+  uint64_t s_full[2], p_full[2], o_done, conv_sync;
+  uint64_t q_free, q_lo_full, q_cp_done, q_hi_full;  // per-sequence Q staging
   uint32_t tmem_base;
   int abort_flag;
+  Plan plan;
   float kscale[kStages][kPage];
 };
 
@@ -70,38 +81,100 @@ __device__ __forceinline__ int clamp_len(int L, int max_pages) {
   return min(max(L, 0), max_pages * kPage);
 }
 
+__device__ __forceinline__ int warp_sum(int v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+// The Plan of work unit `unit`, computed by one warp with coalesced loads of the lengths
+// (256 at a time) and warp scans.
+__device__ void make_plan(const Params& prm, int unit, Plan* out) {
+  const int lane = threadIdx.x & 31;
+  const int B = prm.B;
+  auto pages_at = [&](int bb) {
+    return bb < B ? pages_of(clamp_len(__ldg(prm.cache_lens + bb), prm.max_pages), kPage) : 0;
+  };
+  int total = 0;
+  for (int base = 0; base < B; base += 256) {
+    int n[8], sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) n[i] = pages_at(base + i * 32 + lane);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sum += n[i];
+    total += warp_sum(sum);
+  }
+  const int chunk = total > 0 ? (total + prm.G - 1) / prm.G : 1;
+  const int start = min(total, unit * chunk), end = min(total, start + chunk);
+  int pb = 0, b0 = B, pb0 = total;
+  bool found = false;
+  for (int base = 0; base < B && !found; base += 256) {
+    int n[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) n[i] = pages_at(base + i * 32 + lane);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (found) break;
+      int incl = n[i];
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+      }
+      // the first sequence whose pages end past `start`; every earlier one ends at or before it
+      const int bb = base + i * 32 + lane;
+      const unsigned hit = __ballot_sync(0xffffffffu, bb < B && pb + incl > start);
+      if (hit) {
+        const int first = __ffs(hit) - 1;
+        b0 = base + i * 32 + first;
+        pb0 = pb + __shfl_sync(0xffffffffu, incl - n[i], first);
+        found = true;
+      } else {
+        pb += __shfl_sync(0xffffffffu, incl, 31);
+      }
+    }
+  }
+  if (lane == 0) *out = Plan{start, end, b0, pb0};
+}
+
 // Walks the (sequence, page range) segments of this CTA's work unit in order; every
 // role runs its own copy and sees the same sequence.
 struct Segments {
   const int* lens;
   int B, max_pages, start, end, b, pb;
-  __device__ void init(const Params& prm, int unit) {
+  __device__ void init(const Params& prm, const Plan& plan) {
     lens = prm.cache_lens;
     B = prm.B;
     max_pages = prm.max_pages;
-    int total = 0;
-    for (int i = 0; i < B; ++i) total += pages_of(clamp_len(__ldg(lens + i), max_pages), kPage);
-    const int chunk = total > 0 ? (total + prm.G - 1) / prm.G : 1;
-    start = unit * chunk;
-    end = min(total, start + chunk);
-    b = 0;
-    pb = 0;
+    start = plan.start;
+    end = plan.end;
+    b = plan.b0;
+    pb = plan.pb0;
   }
   // Next non-empty segment: sets seq, L, lo, hi (page indices within the sequence).
+  // Lengths are fetched eight at a time so that skipping to this unit's first sequence
+  // costs one load latency per eight sequences rather than one per sequence.
   __device__ bool next(int& seq, int& L, int& lo, int& hi) {
     while (b < B && pb < end) {
-      const int Lb = clamp_len(__ldg(lens + b), max_pages);
-      const int n = pages_of(Lb, kPage);
-      const int l0 = max(start, pb) - pb, h0 = min(end, pb + n) - pb;
-      const int cur = b;
-      pb += n;
-      ++b;
-      if (l0 < h0) {
-        seq = cur;
-        L = Lb;
-        lo = l0;
-        hi = h0;
-        return true;
+      int Ls[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) Ls[i] = b + i < B ? __ldg(lens + b + i) : 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (b >= B || pb >= end) return false;
+        const int Lb = clamp_len(Ls[i], max_pages);
+        const int n = pages_of(Lb, kPage);
+        const int l0 = max(start, pb) - pb, h0 = min(end, pb + n) - pb;
+        const int cur = b;
+        pb += n;
+        ++b;
+        if (l0 < h0) {
+          seq = cur;
+          L = Lb;
+          lo = l0;
+          hi = h0;
+          return true;
+        }
       }
     }
     return false;
@@ -116,7 +189,9 @@ __device__ __forceinline__ int page_row(const Params& p, int seq, int pg) {
 
 template <bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
-    decode_split_kernel(const __grid_constant__ CUtensorMap tm_cache, const Params p) {
+    decode_split_kernel(const __grid_constant__ CUtensorMap tm_cache,
+                        const __grid_constant__ CUtensorMap tm_qlat,
+                        const __grid_constant__ CUtensorMap tm_qrope, const Params p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -137,28 +212,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&bars.p_full[i], kRows);
     }
     ptx::mbar_init(&bars.o_done, 1);
-    ptx::mbar_init(&bars.q_ready, kRows);
+    ptx::mbar_init(&bars.q_free, 1);
+    ptx::mbar_init(&bars.q_lo_full, 1);
+    ptx::mbar_init(&bars.q_cp_done, 1);
+    ptx::mbar_init(&bars.q_hi_full, 1);
     ptx::mbar_init(&bars.conv_sync, kPrepThreads);
     ptx::fence_barrier_init();
   }
+  // Q rows T*H..127 are never loaded: keep them zero (finite scores in the padded rows)
+  for (int i = threadIdx.x; i < 5 * kQChunk / 16; i += kThreads)
+    reinterpret_cast<uint4*>(sm + kOffQhi)[i] = make_uint4(0, 0, 0, 0);
+  ptx::fence_proxy_async();
   if (warp == 2) ptx::tmem_alloc(&bars.tmem_base, 512);
+  if (warp == 3) make_plan(p, unit, &bars.plan);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
   volatile int* abort_flag = &bars.abort_flag;
   Segments segs;
-  segs.init(p, unit);
+  segs.init(p, bars.plan);
   int seq, L, lo, hi;
 
   if (warp == 0) {
     // -------------------------------------------------------------- TMA producer
     if (ptx::elect_one()) {
       ptx::prefetch_tensormap(&tm_cache);
-      int g = 0;
+      ptx::prefetch_tensormap(&tm_qlat);
+      int g = 0, nseg = 0;
       bool ok = true;
       const int chunk_bytes = kFp8 ? kRawChunk : kPageChunk;
       while (ok && segs.next(seq, L, lo, hi)) {
+        // Q latent 0..255 into the Q area once the previous sequence's last S is done
+        if (nseg > 0 && !(ok = ptx::mbar_wait(&bars.q_free, (nseg - 1) & 1, abort_flag, p.err))) break;
+        ptx::mbar_arrive_expect_tx(&bars.q_lo_full, 4 * TH * 128);
+        for (int c = 0; c < 4; ++c)
+          ptx::tma_load_2d(sm + kOffQhi + c * kQChunk, &tm_qlat, &bars.q_lo_full, c * 64, seq * TH);
+        ++nseg;
         for (int a = lo; a < min(hi, lo + kPrefetchAhead); ++a) {
           const int y = page_row(p, seq, a);
           if (y >= 0)
@@ -216,8 +306,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       while (ok && segs.next(seq, L, lo, hi)) {
-        // Q of this sequence (TMEM + shared memory) is written by the softmax warps
-        if (!(ok = ptx::mbar_wait(&bars.q_ready, nseg & 1, abort_flag, p.err))) break;
+        // Q latent 0..255: staged in the Q area by the producer, copied into TMEM columns
+        // 0..127 (lane = query row); then latent 256..511 + rope over the staging copy
+        if (!(ok = ptx::mbar_wait(&bars.q_lo_full, nseg & 1, abort_flag, p.err))) break;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          ptx::tmem_cp_128x256b(tmem + k * 8, ptx::sw128_desc(qhi + (k >> 2) * kQChunk + (k & 3) * 32, 16, 1024));
+        ptx::mma_commit(&bars.q_cp_done);
+        if (!(ok = ptx::mbar_wait(&bars.q_cp_done, nseg & 1, abort_flag, p.err))) break;
+        ptx::mbar_arrive_expect_tx(&bars.q_hi_full, 5 * TH * 128);
+        for (int c = 0; c < 4; ++c)
+          ptx::tma_load_2d(sm + kOffQhi + c * kQChunk, &tm_qlat, &bars.q_hi_full, 256 + c * 64, seq * TH);
+        ptx::tma_load_2d(sm + kOffQhi + 4 * kQChunk, &tm_qrope, &bars.q_hi_full, 0, seq * TH);
+        if (!(ok = ptx::mbar_wait(&bars.q_hi_full, nseg & 1, abort_flag, p.err))) break;
         ptx::tc_fence_after();
         const int g_end = g + (hi - lo), g_first = g;
         int gs = g, gp = g;  // next page whose S / whose PV is to be issued
@@ -231,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             issue_s(gs);
             ptx::mma_commit(&bars.s_full[gs & 1]);
             ++gs;
+            if (gs == g_end) ptx::mma_commit(&bars.q_free);  // Q no longer read
             progress = true;
           }
           if (gp < gs && ptx::mbar_test_wait(&bars.p_full[gp & 1], (gp >> 1) & 1)) {
@@ -330,53 +433,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // -------------------------------------------------------------- softmax / Q / epilogue
+    // -------------------------------------------------------------- softmax / epilogue
     const int r = threadIdx.x - 128;  // query row == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int t_row = r / p.H;
     int g = 0;
     bool ok = true;
     while (ok && segs.next(seq, L, lo, hi)) {
-      // the previous segment's MMAs are done (its epilogue waited for the last PV), so
-      // Q can be overwritten: latent 0..255 -> TMEM columns 0..127, the rest -> smem
-      {
-        const bool live = r < TH;
-        const size_t qrow = (size_t)seq * TH + r;
-        const uint4* ql = reinterpret_cast<const uint4*>(p.q_latent + qrow * kDl);
-        const uint4* qr = reinterpret_cast<const uint4*>(p.q_rope + qrow * 64);
-        {  // latent 0..255: all 32 loads in flight, then 4 x 32 TMEM columns
-          uint32_t v[4][32];
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int x = 0; x < 8; ++x) {
-              const uint4 u = live ? __ldg(ql + c * 8 + x) : make_uint4(0, 0, 0, 0);
-              v[c][4 * x] = u.x; v[c][4 * x + 1] = u.y; v[c][4 * x + 2] = u.z; v[c][4 * x + 3] = u.w;
-            }
-#pragma unroll
-          for (int c = 0; c < 4; ++c) ptx::tmem_st32(tmem + lane_off + c * 32, v[c]);
-        }
-#pragma unroll
-        for (int half_q = 0; half_q < 2; ++half_q) {  // latent 256..511 (4 chunks) + rope
-          const int c0 = half_q * 2, c1 = half_q ? 5 : 2;
-          uint4 u[3][8];
-#pragma unroll
-          for (int c = c0; c < c1; ++c)
-#pragma unroll
-            for (int x = 0; x < 8; ++x)
-              u[c - c0][x] = !live ? make_uint4(0, 0, 0, 0) : (c < 4 ? __ldg(ql + 32 + c * 8 + x) : __ldg(qr + x));
-#pragma unroll
-          for (int c = c0; c < c1; ++c) {
-            unsigned char* dst = sm + kOffQhi + c * kQChunk + r * 128;
-#pragma unroll
-            for (int x = 0; x < 8; ++x) *reinterpret_cast<uint4*>(dst + ((x ^ (r & 7)) << 4)) = u[c - c0][x];
-          }
-        }
-        ptx::tmem_st_wait();
-        ptx::fence_proxy_async();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(&bars.q_ready);
-      }
       const int last_visible = p.causal ? (L - p.T + t_row) : (L - 1);  // keys <= this are visible
       float m = -INFINITY, l = 0.f, lr = 0.f;  // exact row sum (LSE) and bf16-rounded (PV)
       const uint32_t o_addr = tmem + lane_off + 256;
@@ -472,7 +535,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_after();
       const size_t slot = (size_t)unit + seq;
       const float inv = lr > 0.f ? 1.f / lr : 0.f;
-      float* dst = p.part_o + (slot * TH + r) * kDl + half * 256;
+      // partial layout [slot][column quad (128)][row (T*H)][4]: the 32 rows of a warp
+      // store one quad as 512 contiguous bytes
+      float4* dst = reinterpret_cast<float4*>(p.part_o) + (slot * 128 + half * 64) * TH + r;
 #pragma unroll 1
       for (int c = 0; c < 8; c += 2) {
         uint32_t v[2][32];
@@ -484,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
             for (int x = 0; x < 8; ++x)
-              reinterpret_cast<float4*>(dst + (c + h2) * 32)[x] =
+              dst[(size_t)((c + h2) * 8 + x) * TH] =
                   make_float4(__uint_as_float(v[h2][4 * x]) * inv, __uint_as_float(v[h2][4 * x + 1]) * inv,
                               __uint_as_float(v[h2][4 * x + 2]) * inv, __uint_as_float(v[h2][4 * x + 3]) * inv);
         }
@@ -526,6 +591,19 @@ cudaError_t launch_decode_sm103(const void* q_latent, const void* q_rope, const 
       &tm, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_cache,
       dims, strides, box, /*swizzle128=*/!fp8);
   if (e != cudaSuccess) return e;
+  // Q as 2-D tensors [B*T*H rows, 512 | 64 columns]; boxes of 64 columns x T*H rows
+  // (one sequence), 128B-swizzled like the operand tiles
+  const int TH = T * H;
+  CUtensorMap tm_qlat, tm_qrope;
+  uint64_t qdims[2] = {(uint64_t)kDl, (uint64_t)B * TH};
+  uint64_t qstrides[1] = {(uint64_t)kDl * 2};
+  uint32_t qbox[2] = {64, (uint32_t)TH};
+  e = encode_tensor_map_swz(&tm_qlat, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q_latent, qdims, qstrides, qbox, true);
+  if (e != cudaSuccess) return e;
+  qdims[0] = 64;
+  qstrides[0] = 128;
+  e = encode_tensor_map_swz(&tm_qrope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q_rope, qdims, qstrides, qbox, true);
+  if (e != cudaSuccess) return e;
   Params p;
   p.q_latent = static_cast<const uint16_t*>(q_latent);
   p.q_rope = static_cast<const uint16_t*>(q_rope);
@@ -550,7 +628,7 @@ cudaError_t launch_decode_sm103(const void* q_latent, const void* q_rope, const 
       if (e2 != cudaSuccess) return e2;
       checked[fp8 ? 1 : 0] = true;
     }
-    kern<<<2 * G, kThreads, kSmemAlloc, stream>>>(tm, p);
+    kern<<<2 * G, kThreads, kSmemAlloc, stream>>>(tm, tm_qlat, tm_qrope, p);
     return cudaGetLastError();
   };
   return fp8 ? go(decode_split_kernel<true>) : go(decode_split_kernel<false>);

@@ -199,6 +199,13 @@ __device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
+// Copy 128 rows x 256 bits from a shared-memory matrix (descriptor as for the MMA
+// operands) into TMEM: row i lands in lane i, eight consecutive 32-bit columns from taddr.
+// Asynchronous like the MMA; completion is tracked by mma_commit.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(desc));
+}
+
 // Arrive once on `bar` when every tcgen05 operation issued so far by this thread is done.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
