@@ -9,17 +9,20 @@
 namespace mla {
 
 constexpr int kCombDl = 512, kCombPage = 64;
-constexpr int kCombRows = 32;    // query rows per CTA: one per lane
-constexpr int kCombWarps = 8;    // each warp merges every 8th column quad of those rows
-constexpr int kCombMaxSplits = 80;   // split weights of one sequence kept in shared memory
+constexpr int kCombRows = 32;        // query rows per CTA: one per lane
+constexpr int kCombWarps = 8;
+constexpr int kCombParts = 4;        // CTAs per row group, each merging 128 of the 512 columns
+constexpr int kCombQuads = kCombDl / 4 / kCombParts;  // 32 column quads per CTA, 4 per warp
 
 __device__ __forceinline__ int comb_clamp_len(int L, int max_pages) {
   return min(max(L, 0), max_pages * kCombPage);
 }
 
 // Partials are laid out [slot][column quad q (128)][row (T*H)][4 floats]; lane = row, so
-// every load of a warp is 512 contiguous bytes.  The bf16 rows are assembled in shared
-// memory and written out row by row.
+// every load of a warp is 512 contiguous bytes.  CTA (b, row group, part) merges quads
+// [32 part, 32 part + 32) of 32 rows; each warp keeps 4 quads x 2 splits of loads in
+// flight, and each thread weighs the splits of its own row from their LSEs.  The bf16
+// rows are assembled in shared memory and written out row by row.
 __global__ void __launch_bounds__(kCombWarps * 32) decode_combine_kernel(
     const float* __restrict__ part_o, const float* __restrict__ part_lse,
     const int* __restrict__ cache_lens, uint16_t* __restrict__ out, float* __restrict__ lse,
@@ -28,10 +31,9 @@ __global__ void __launch_bounds__(kCombWarps * 32) decode_combine_kernel(
   const int TH = T * H;
   const int row0 = blockIdx.y * kCombRows;
   const int nrows = min(kCombRows, TH - row0);
+  const int q_base = blockIdx.z * kCombQuads;
   __shared__ int s_pb, s_n, s_chunk;
-  __shared__ float s_w[kCombMaxSplits][kCombRows];  // exp(lse_s - max) / sum
-  __shared__ float s_mx[kCombRows], s_inv[kCombRows];
-  __shared__ __align__(16) uint16_t s_out[kCombRows][kCombDl];
+  __shared__ __align__(16) uint16_t s_out[kCombRows][kCombQuads * 4];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == 0) {
     // pages of sequences before b and in total, 32 lengths at a time
@@ -61,64 +63,69 @@ __global__ void __launch_bounds__(kCombWarps * 32) decode_combine_kernel(
   const int nsplit = c_last - c_first + 1;
   const int row = row0 + lane;
   const bool live = lane < nrows;
-  // weights of the splits, per row: w_s = exp(lse_s - max) / sum
+  constexpr int kQ = kCombQuads / kCombWarps;  // quads per warp
+  float4 acc[kQ];
+#pragma unroll
+  for (int j = 0; j < kQ; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
   float mx = -INFINITY, wsum = 0.f;
-  if (warp == 0 && live) {
-    for (int c = c_first; c <= c_last; ++c) mx = fmaxf(mx, __ldg(part_lse + ((size_t)c + b) * TH + row));
-    for (int c = c_first; c <= c_last; ++c) {
-      const float ls = __ldg(part_lse + ((size_t)c + b) * TH + row);
-      const float w = (mx == -INFINITY || ls == -INFINITY) ? 0.f : __expf(ls - mx);
-      wsum += w;
-      if (c - c_first < kCombMaxSplits) s_w[c - c_first][lane] = w;
+  if (live && nsplit > 0) {
+    // every thread weighs the splits of its own row: w_s = exp(lse_s - max) / sum; the
+    // partial loads of the first two splits are issued before the weights are known
+    const size_t slot_stride = (size_t)128 * TH;
+    const float4* src = reinterpret_cast<const float4*>(part_o) +
+                        ((size_t)(c_first + b) * 128 + q_base + warp) * TH + row;
+    const float* lsp = part_lse + ((size_t)c_first + b) * TH + row;
+    float4 a[2][kQ];
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+      for (int j = 0; j < kQ; ++j)
+        a[u][j] = u < nsplit ? __ldg(src + (size_t)u * slot_stride + (size_t)j * kCombWarps * TH)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < nsplit; ++k) mx = fmaxf(mx, __ldg(lsp + (size_t)k * TH));
+    for (int k = 0; k < nsplit; ++k) {
+      const float ls = __ldg(lsp + (size_t)k * TH);
+      wsum += (mx == -INFINITY || ls == -INFINITY) ? 0.f : __expf(ls - mx);
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    for (int k = 0; k < min(nsplit, kCombMaxSplits); ++k) s_w[k][lane] *= inv;
-    s_mx[lane] = mx;
-    s_inv[lane] = inv;
-    lse[((size_t)b * H + row % H) * T + row / H] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
-  }
-  __syncthreads();
-  // weight of split k of this lane's row (beyond the shared-memory table: from its LSE)
-  auto weight = [&](int k) -> float {
-    if (k < kCombMaxSplits) return s_w[k][lane];
-    const float ls = __ldg(part_lse + ((size_t)(c_first + k) + b) * TH + row);
-    return (s_mx[lane] == -INFINITY || ls == -INFINITY) ? 0.f : __expf(ls - s_mx[lane]) * s_inv[lane];
-  };
-  for (int q = warp; q < kCombDl / 4; q += kCombWarps) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (live) {
-      const float4* src = reinterpret_cast<const float4*>(part_o) + ((size_t)(c_first + b) * 128 + q) * TH + row;
-      const size_t slot_stride = (size_t)128 * TH;
-      int k = 0;
-      for (; k + 4 <= nsplit; k += 4) {  // four splits in flight
-        float4 a[4];
+    auto weight = [&](int k) -> float {
+      const float ls = __ldg(lsp + (size_t)k * TH);
+      return (mx == -INFINITY || ls == -INFINITY) ? 0.f : __expf(ls - mx) * inv;
+    };
+    for (int k = 0; k < nsplit; k += 2) {
+      if (k > 0) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) a[u] = __ldg(src + (size_t)(k + u) * slot_stride);
+        for (int u = 0; u < 2; ++u)
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float w = weight(k + u);
-          if (w != 0.f) {
-            acc.x += w * a[u].x; acc.y += w * a[u].y; acc.z += w * a[u].z; acc.w += w * a[u].w;
-          }
-        }
+          for (int j = 0; j < kQ; ++j)
+            a[u][j] = k + u < nsplit ? __ldg(src + (size_t)(k + u) * slot_stride + (size_t)j * kCombWarps * TH)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      for (; k < nsplit; ++k) {
-        const float4 a = __ldg(src + (size_t)k * slot_stride);
-        const float w = weight(k);
-        if (w != 0.f) {
-          acc.x += w * a.x; acc.y += w * a.y; acc.z += w * a.z; acc.w += w * a.w;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const float w = k + u < nsplit ? weight(k + u) : 0.f;
+#pragma unroll
+        for (int j = 0; j < kQ; ++j) {
+          acc[j].x += w * a[u][j].x; acc[j].y += w * a[u][j].y;
+          acc[j].z += w * a[u][j].z; acc[j].w += w * a[u][j].w;
         }
       }
     }
-    const uint32_t lo = (uint32_t)f32_to_bf16_rne(acc.x) | ((uint32_t)f32_to_bf16_rne(acc.y) << 16);
-    const uint32_t hi = (uint32_t)f32_to_bf16_rne(acc.z) | ((uint32_t)f32_to_bf16_rne(acc.w) << 16);
-    *reinterpret_cast<uint2*>(&s_out[lane][q * 4]) = make_uint2(lo, hi);
+  }
+  if (live && warp == 0 && blockIdx.z == 0)
+    lse[((size_t)b * H + row % H) * T + row / H] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+#pragma unroll
+  for (int j = 0; j < kQ; ++j) {
+    const int ql = warp + j * kCombWarps;  // quad within this CTA's 32
+    const uint32_t lo = (uint32_t)f32_to_bf16_rne(acc[j].x) | ((uint32_t)f32_to_bf16_rne(acc[j].y) << 16);
+    const uint32_t hi = (uint32_t)f32_to_bf16_rne(acc[j].z) | ((uint32_t)f32_to_bf16_rne(acc[j].w) << 16);
+    *reinterpret_cast<uint2*>(&s_out[lane][ql * 4]) = make_uint2(lo, hi);
   }
   __syncthreads();
-  // rows out: 64 x 16 bytes each
-  for (int i = threadIdx.x; i < nrows * (kCombDl / 8); i += kCombWarps * 32) {
-    const int rr = i / (kCombDl / 8), cc = i % (kCombDl / 8);
-    reinterpret_cast<uint4*>(out + ((size_t)b * TH + row0 + rr) * kCombDl)[cc] =
+  // rows out: this CTA's 128 columns of each row are 16 x 16 bytes
+  for (int i = threadIdx.x; i < nrows * 16; i += kCombWarps * 32) {
+    const int rr = i >> 4, cc = i & 15;
+    reinterpret_cast<uint4*>(out + ((size_t)b * TH + row0 + rr) * kCombDl + q_base * 4)[cc] =
         reinterpret_cast<const uint4*>(&s_out[rr][0])[cc];
   }
 }
@@ -127,7 +134,7 @@ cudaError_t launch_decode_combine(const float* part_o, const float* part_lse,
                                   const int* cache_lens, void* out, float* lse, int B, int H,
                                   int T, int max_pages, int G, cudaStream_t stream) {
   const int TH = T * H;
-  dim3 grid(B, (TH + kCombRows - 1) / kCombRows);
+  dim3 grid(B, (TH + kCombRows - 1) / kCombRows, kCombParts);
   decode_combine_kernel<<<grid, kCombWarps * 32, 0, stream>>>(part_o, part_lse, cache_lens,
                                                   static_cast<uint16_t*>(out), lse, B, H, T,
                                                   max_pages, G);
