@@ -19,7 +19,8 @@
 //               with P read from TMEM.  S(g+1) and PV(g) are issued in whichever order their
 //               inputs arrive.
 //   warps 2-3   stage preparation: zero the rows past the sequence end of a partial page;
-//               fp8: widen the page to bf16 in place (chunk by chunk) and stage its scales
+//   (+ 8-11)    fp8: widen the page to bf16 in place (three chunks of one row per thread;
+//               warps 8-11 exist in the fp8 kernel only) and stage its scales
 //   warps 4-7   softmax, one thread per query row; they also write the split's partial
 //               (O_half / l, log-sum-exp), column quads of 32 rows per 512-byte store
 // TMEM columns: [0,128) Q latent 0..255 (bf16 pairs), [128,256) two S / P buffers of 64,
@@ -44,8 +45,9 @@ constexpr int kOffQhi = 0;                    // latent 256..511 (4 chunks) + ro
 constexpr int kOffStage = 5 * kQChunk;        // 80 KB
 constexpr int kSmemBytes = kOffStage + kStages * kStageBytes;  // 224 KB
 constexpr int kSmemAlloc = kSmemBytes + 1024;
-constexpr int kThreads = 256;
-constexpr int kPrepThreads = 64;
+// bf16: 8 warps; fp8: 12 (four more page-widening warps)
+template <bool kFp8> constexpr int kThreadsOf = kFp8 ? 384 : 256;
+template <bool kFp8> constexpr int kPrepOf = kFp8 ? 192 : 64;
 constexpr int kPrefetchAhead = 4;             // pages warmed in L2 ahead of their load
 
 struct Params {
@@ -188,7 +190,7 @@ __device__ __forceinline__ int page_row(const Params& p, int seq, int pg) {
 }
 
 template <bool kFp8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_cache,
                         const __grid_constant__ CUtensorMap tm_qlat,
                         const __grid_constant__ CUtensorMap tm_qrope, const Params p) {
@@ -196,6 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   __shared__ Bars bars;
+  constexpr int kThreads = kThreadsOf<kFp8>, kPrepThreads = kPrepOf<kFp8>;
   const int warp = threadIdx.x >> 5;
   const int unit = blockIdx.x >> 1, half = blockIdx.x & 1;
   const int TH = p.T * p.H;
@@ -243,30 +246,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       const int chunk_bytes = kFp8 ? kRawChunk : kPageChunk;
       while (ok && segs.next(seq, L, lo, hi)) {
-        // Q latent 0..255 into the Q area once the previous sequence's last S is done
-        if (nseg > 0 && !(ok = ptx::mbar_wait(&bars.q_free, (nseg - 1) & 1, abort_flag, p.err))) break;
-        ptx::mbar_arrive_expect_tx(&bars.q_lo_full, 4 * TH * 128);
-        for (int c = 0; c < 4; ++c)
-          ptx::tma_load_2d(sm + kOffQhi + c * kQChunk, &tm_qlat, &bars.q_lo_full, c * 64, seq * TH);
-        ++nseg;
-        for (int a = lo; a < min(hi, lo + kPrefetchAhead); ++a) {
-          const int y = page_row(p, seq, a);
-          if (y >= 0)
-            for (int c = 0; c < 9; ++c) ptx::tma_prefetch_2d(&tm_cache, c * 64, y);
+        if (nseg == 0) {
+          // first sequence: Q latent 0..255 staged in the (still unused) second page stage,
+          // the rest of Q straight into the Q area, all at once
+          ptx::mbar_arrive_expect_tx(&bars.q_lo_full, 4 * TH * 128);
+          for (int c = 0; c < 4; ++c)
+            ptx::tma_load_2d(sm + kOffStage + kStageBytes + c * kQChunk, &tm_qlat, &bars.q_lo_full, c * 64, seq * TH);
+          ptx::mbar_arrive_expect_tx(&bars.q_hi_full, 5 * TH * 128);
+          for (int c = 0; c < 4; ++c)
+            ptx::tma_load_2d(sm + kOffQhi + c * kQChunk, &tm_qlat, &bars.q_hi_full, 256 + c * 64, seq * TH);
+          ptx::tma_load_2d(sm + kOffQhi + 4 * kQChunk, &tm_qrope, &bars.q_hi_full, 0, seq * TH);
+        } else {
+          // Q latent 0..255 into the Q area once the previous sequence's last S is done
+          if (!(ok = ptx::mbar_wait(&bars.q_free, (nseg - 1) & 1, abort_flag, p.err))) break;
+          ptx::mbar_arrive_expect_tx(&bars.q_lo_full, 4 * TH * 128);
+          for (int c = 0; c < 4; ++c)
+            ptx::tma_load_2d(sm + kOffQhi + c * kQChunk, &tm_qlat, &bars.q_lo_full, c * 64, seq * TH);
         }
+        ++nseg;
         for (int pg = lo; pg < hi; ++pg, ++g) {
-          if (pg + kPrefetchAhead < hi) {
-            const int ya = page_row(p, seq, pg + kPrefetchAhead);
-            if (ya >= 0)
-              for (int c = 0; c < 9; ++c) ptx::tma_prefetch_2d(&tm_cache, c * 64, ya);
-          }
           const int s = g % kStages;
           if (!(ok = ptx::mbar_wait(&bars.stage_empty[s], ((g / kStages) & 1) ^ 1, abort_flag, p.err))) break;
+          // the second stage holds the first sequence's staged Q until it is copied to TMEM
+          // (when page 1 belongs to a later sequence, that sequence's wait for q_free
+          // already implied the copy: it precedes the first sequence's MMAs)
+          if (g == 1 && nseg == 1 && !(ok = ptx::mbar_wait(&bars.q_cp_done, 0, abort_flag, p.err))) break;
           const int y = page_row(p, seq, pg);
           unsigned char* dst = sm + kOffStage + s * kStageBytes + (kFp8 ? kRawOffset : 0);
           ptx::mbar_arrive_expect_tx(&bars.stage_full[s], 9 * chunk_bytes);
           for (int c = 0; c < 9; ++c)
             ptx::tma_load_2d(dst + c * chunk_bytes, &tm_cache, &bars.stage_full[s], c * 64, y);
+          // warm L2 with the pages ahead (after this page's own load has been issued)
+          for (int a = (pg == lo ? lo + 1 : pg + kPrefetchAhead); a <= min(hi - 1, pg + kPrefetchAhead); ++a) {
+            const int ya = page_row(p, seq, a);
+            if (ya >= 0)
+              for (int c = 0; c < 9; ++c) ptx::tma_prefetch_2d(&tm_cache, c * 64, ya);
+          }
         }
       }
     }
@@ -310,15 +325,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 0..127 (lane = query row); then latent 256..511 + rope over the staging copy
         if (!(ok = ptx::mbar_wait(&bars.q_lo_full, nseg & 1, abort_flag, p.err))) break;
         ptx::tc_fence_after();
+        // the first sequence's Q latent 0..255 was staged in the second page stage
+        const uint32_t q_stage = nseg == 0 ? stage0 + kStageBytes : qhi;
 #pragma unroll
         for (int k = 0; k < 16; ++k)
-          ptx::tmem_cp_128x256b(tmem + k * 8, ptx::sw128_desc(qhi + (k >> 2) * kQChunk + (k & 3) * 32, 16, 1024));
+          ptx::tmem_cp_128x256b(tmem + k * 8, ptx::sw128_desc(q_stage + (k >> 2) * kQChunk + (k & 3) * 32, 16, 1024));
         ptx::mma_commit(&bars.q_cp_done);
-        if (!(ok = ptx::mbar_wait(&bars.q_cp_done, nseg & 1, abort_flag, p.err))) break;
-        ptx::mbar_arrive_expect_tx(&bars.q_hi_full, 5 * TH * 128);
-        for (int c = 0; c < 4; ++c)
-          ptx::tma_load_2d(sm + kOffQhi + c * kQChunk, &tm_qlat, &bars.q_hi_full, 256 + c * 64, seq * TH);
-        ptx::tma_load_2d(sm + kOffQhi + 4 * kQChunk, &tm_qrope, &bars.q_hi_full, 0, seq * TH);
+        if (nseg > 0) {  // the rest of Q over the staging copy (the producer loaded the first)
+          if (!(ok = ptx::mbar_wait(&bars.q_cp_done, nseg & 1, abort_flag, p.err))) break;
+          ptx::mbar_arrive_expect_tx(&bars.q_hi_full, 5 * TH * 128);
+          for (int c = 0; c < 4; ++c)
+            ptx::tma_load_2d(sm + kOffQhi + c * kQChunk, &tm_qlat, &bars.q_hi_full, 256 + c * 64, seq * TH);
+          ptx::tma_load_2d(sm + kOffQhi + 4 * kQChunk, &tm_qrope, &bars.q_hi_full, 0, seq * TH);
+        }
         if (!(ok = ptx::mbar_wait(&bars.q_hi_full, nseg & 1, abort_flag, p.err))) break;
         ptx::tc_fence_after();
         const int g_end = g + (hi - lo), g_first = g;
@@ -360,9 +379,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++nseg;
       }
     }
-  } else if (warp < 4) {
+  } else if (warp < 4 || warp >= 8) {
     // -------------------------------------------------------------- stage preparation
-    const int tid = threadIdx.x - 64;  // 0..63: one page row each
+    const int tid = warp < 4 ? threadIdx.x - 64 : threadIdx.x - 192;  // 0 .. kPrepThreads-1
+    const int row = tid & (kPage - 1);  // fp8: page row; thread group tid / 64 widens
+                                        // chunks 3 (tid / 64) .. 3 (tid / 64) + 2 of it
     int g = 0;
     bool ok = true;
     while (ok && segs.next(seq, L, lo, hi)) {
@@ -373,9 +394,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int page = __ldg(p.page_table + (size_t)seq * p.max_pages + pg);
         const bool bad = page < 0 || page >= p.num_pages;
         if (bad && tid == 0) latch_error(p.err, kErrBadPage);
-        const bool live = !bad && tid < valid;
+        const bool live = !bad && row < valid;
         float ksc = 0.f;
-        if constexpr (kFp8) ksc = live ? __ldg(p.kv_scale + (size_t)page * kPage + tid) : 0.f;
+        if constexpr (kFp8) ksc = live && tid < kPage ? __ldg(p.kv_scale + (size_t)page * kPage + row) : 0.f;
         ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.stage_full[s], (g / kStages) & 1, abort_flag, p.err));
         if (!ok) break;
         if constexpr (!kFp8) {
@@ -388,14 +409,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         } else {
-          bars.kscale[s][tid] = ksc;
-          // Widen in place.  bf16 chunk c (bytes [8c, 8c+8) KB) overlaps raw chunks 2c-9 and
-          // 2c-8 (raw chunk c' sits at [36 + 4c', 40 + 4c') KB), so chunks 0..3 land below the
-          // raw bytes and can be written at once, while chunks 4..8 overwrite raw bytes other
-          // threads may still be reading: every thread first holds its raw rows of chunks
-          // 4..8 in registers, then all 64 threads meet (bounded mbarrier), then write.
-          const int row = tid;
-          auto widen = [&](const uint4 (&raw)[4], int c) {
+          if (tid < kPage) bars.kscale[s][row] = ksc;
+          // Widen in place, in three lockstep steps of three chunks (one chunk row per
+          // thread per step).  bf16 chunk c (bytes [8c, 8c+8) KB) overlaps raw chunks 2c-9
+          // and 2c-8 (raw chunk c' sits at [36 + 4c', 40 + 4c') KB), which are at most the
+          // step's own chunks 3k..3k+2 or earlier ones: after every thread has read its raw
+          // row of the step (bounded mbarrier), the step's writes only destroy bytes that
+          // were already read, and never those of a later step.
+          const int cgrp = tid >> 6;
+#pragma unroll 1
+          for (int k = 0; k < 3 && ok; ++k) {
+            const int c = 3 * k + cgrp;
+            const uint4* src = reinterpret_cast<const uint4*>(st + kRawOffset + c * kRawChunk + row * 64);
+            uint4 raw[4];
+#pragma unroll
+            for (int x = 0; x < 4; ++x) raw[x] = live ? src[x] : make_uint4(0, 0, 0, 0);
+            ptx::mbar_arrive(&bars.conv_sync);
+            ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.conv_sync, (3 * g + k) & 1, abort_flag, p.err));
+            if (!ok) break;
             const uint8_t* bytes = reinterpret_cast<const uint8_t*>(raw);
             unsigned char* dst = st + c * kPageChunk + row * 128;
 #pragma unroll
@@ -407,26 +438,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         e4m3_to_f32(bytes[gr * 8 + 2 * x + 1]));
               *reinterpret_cast<uint4*>(dst + ((gr ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
-          };
-          auto load_raw = [&](uint4 (&raw)[4], int c) {
-            const uint4* src = reinterpret_cast<const uint4*>(st + kRawOffset + c * kRawChunk + row * 64);
-#pragma unroll
-            for (int x = 0; x < 4; ++x) raw[x] = live ? src[x] : make_uint4(0, 0, 0, 0);
-          };
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint4 raw[4];
-            load_raw(raw, c);
-            widen(raw, c);
           }
-          uint4 hold[5][4];
-#pragma unroll
-          for (int c = 4; c < 9; ++c) load_raw(hold[c - 4], c);
-          ptx::mbar_arrive(&bars.conv_sync);
-          ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.conv_sync, g & 1, abort_flag, p.err));
           if (!ok) break;
-#pragma unroll
-          for (int c = 4; c < 9; ++c) widen(hold[c - 4], c);
         }
         ptx::fence_proxy_async();
         ptx::mbar_arrive(&bars.stage_ready[s]);
@@ -624,11 +637,12 @@ cudaError_t launch_decode_sm103(const void* q_latent, const void* q_rope, const 
   auto go = [&](auto kern) -> cudaError_t {
     static bool checked[2] = {false, false};
     if (!checked[fp8 ? 1 : 0]) {
+
       cudaError_t e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
       if (e2 != cudaSuccess) return e2;
       checked[fp8 ? 1 : 0] = true;
     }
-    kern<<<2 * G, kThreads, kSmemAlloc, stream>>>(tm, tm_qlat, tm_qrope, p);
+    kern<<<2 * G, fp8 ? kThreadsOf<true> : kThreadsOf<false>, kSmemAlloc, stream>>>(tm, tm_qlat, tm_qrope, p);
     return cudaGetLastError();
   };
   return fp8 ? go(decode_split_kernel<true>) : go(decode_split_kernel<false>);
