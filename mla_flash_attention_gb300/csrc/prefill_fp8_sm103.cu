@@ -9,11 +9,13 @@
 // MMAs), keeping ~16 significant bits -- O reaches |O| ~ 40 on the fp8 workload and is
 // accumulated and (by default) written in fp32.
 //
-// One CTA = (batch, head, 256 query rows as two 128-row tiles), keys in tiles of 64.  TMEM
-// per Q tile t: [t*256, +64) Sn (later P' high | P' low), [+64, +128) Sr, [+128, +256) O.
-// Roles (12 warps): warp 0 TMA producer (4-stage rings); warp 1 MMA issuer; warps 2-3
-// converters (V8 -> bf16 into a 128B-swizzled N-major tile, key scales into smem);
-// warps 4-7 / 8-11 softmax of Q tiles 0 / 1.
+// One CTA = (batch, head, 128 query rows), keys in tiles of 64.  The score buffers are
+// double-buffered so that S(j+1) runs on the tensor cores while the softmax of tile j runs.
+// TMEM: Sn buffers [0,64) [64,128) (later P' of the tile), Sr buffers [128,192) [192,256),
+// O [256,384).  Roles (14 warps): warp 0 TMA producer (4-stage rings); warp 1 MMA issuer;
+// warps 2-3 and 12-13 converters (V8 -> bf16 into a 128B-swizzled N-major tile, key scales
+// into smem); softmax warpgroups 4-7 and 8-11 take keys 0..31 and 32..63 of every tile for
+// the same 128 rows, and agree on the running row maximum through shared memory.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -23,20 +25,21 @@
 namespace mla {
 namespace sm103_prefill_fp8 {
 
-constexpr int BM = 128, BN = 64, NQ = 2;
+constexpr int BM = 128, BN = 64, KH = 32;   // KH: keys of a tile per softmax warpgroup
 constexpr int kQChunk = BM * 128;          // 128 rows x 128 bytes
 constexpr int kKChunk = BN * 128;          // 64 rows x 128 bytes
 constexpr int kStages = 4;
-constexpr int kOffQn = 0;                                  // NQ x 16 KB (fp8 nope)
-constexpr int kOffQr = kOffQn + NQ * kQChunk;              // NQ x 16 KB (bf16 rope)
-constexpr int kOffKn = kOffQr + NQ * kQChunk;              // stages x 8 KB
+constexpr int kOffQn = 0;                                  // 16 KB (fp8 nope)
+constexpr int kOffQr = kOffQn + kQChunk;                   // 16 KB (bf16 rope)
+constexpr int kOffKn = kOffQr + kQChunk;                   // stages x 8 KB
 constexpr int kOffKr = kOffKn + kStages * kKChunk;         // stages x 8 KB
 constexpr int kOffV8 = kOffKr + kStages * kKChunk;         // stages x 8 KB
 constexpr int kOffVb = kOffV8 + kStages * kKChunk;         // stages x 16 KB (2 chunks)
-constexpr int kSmemBytes = kOffVb + kStages * 2 * kKChunk; // 64 + 160 = 224 KB
+constexpr int kSmemBytes = kOffVb + kStages * 2 * kKChunk; // 32 + 160 = 192 KB
 constexpr int kSmemAlloc = kSmemBytes + 1024;
-constexpr int kThreads = 384;
-constexpr int kConvThreads = 64;
+constexpr int kThreads = 448;
+constexpr int kConvThreads = 128;
+constexpr int kSoftWarps = 8;
 
 struct Params {
   int B, H, S, causal, nrb, out_f32;
@@ -53,15 +56,18 @@ struct Bars {
   uint64_t k_full[kStages], k_empty[kStages];
   uint64_t v8_full[kStages], v8_empty[kStages], vb_full[kStages], vb_empty[kStages];
   uint64_t ks_full[kStages];
-  uint64_t s_full[NQ], p_full[NQ], o_done[NQ];
+  uint64_t s_full[2], p_full[2], o_done;
+  uint64_t mx_bar[2], l_bar;  // the two warpgroups' partial row maxima / row sums are in
   uint32_t tmem_base;
   int abort_flag;
   float ks[kStages][BN];
+  float mx_part[2][2][BM];    // [tile parity][warpgroup][row]
+  float l_part[2][BM];
 };
 
 __device__ __forceinline__ int n_kv_tiles(const Params& p, int q_row0) {
   const int all = (p.S + BN - 1) / BN;
-  return p.causal ? min(all, (q_row0 + NQ * BM + BN - 1) / BN) : all;
+  return p.causal ? min(all, (q_row0 + BM + BN - 1) / BN) : all;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -78,12 +84,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int bid = blockIdx.x;
   const int bh = bid / p.nrb;
-  const int rb = p.nrb - 1 - (bid % p.nrb);
+  const int rb = p.nrb - 1 - (bid % p.nrb);  // longest row blocks first
   const int b = bh / p.H, h = bh % p.H;
-  const int q_row0 = rb * NQ * BM;
+  const int q_row0 = rb * BM;
   const int n_kv = n_kv_tiles(p, q_row0);
-  // causal: Q tile 0 never sees the key tiles past its own rows (above the diagonal)
-  const int n_kv0 = p.causal ? min(n_kv, (q_row0 + BM + BN - 1) / BN) : n_kv;
 
   if (threadIdx.x == 0) {
     bars.abort_flag = 0;
@@ -97,11 +101,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&bars.vb_empty[i], 1);
       ptx::mbar_init(&bars.ks_full[i], kConvThreads);
     }
-    for (int t = 0; t < NQ; ++t) {
+    for (int t = 0; t < 2; ++t) {
       ptx::mbar_init(&bars.s_full[t], 1);
-      ptx::mbar_init(&bars.p_full[t], BM);
-      ptx::mbar_init(&bars.o_done[t], 1);
+      ptx::mbar_init(&bars.p_full[t], kSoftWarps);
+      ptx::mbar_init(&bars.mx_bar[t], kSoftWarps);
     }
+    ptx::mbar_init(&bars.o_done, 1);
+    ptx::mbar_init(&bars.l_bar, kSoftWarps);
     ptx::fence_barrier_init();
   }
   if (warp == 2) ptx::tmem_alloc(&bars.tmem_base, 512);
@@ -111,208 +117,176 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars.tmem_base;
   volatile int* abort_flag = &bars.abort_flag;
 
-  if (warp < 4) {
-    ptx::regs_dec<56>();
-    if (warp == 0) {
-      // ------------------------------------------------------------ producer
-      if (ptx::elect_one()) {
-        ptx::mbar_arrive_expect_tx(&bars.q_full, NQ * 2 * kQChunk);
-        for (int t = 0; t < NQ; ++t) {
-          const int row = q_row0 + t * BM;
-          ptx::tma_load_4d(sm + kOffQn + t * kQChunk, &tm_qn, &bars.q_full, 0, h, row, b);
-          ptx::tma_load_4d(sm + kOffQr + t * kQChunk, &tm_qr, &bars.q_full, 0, h, row, b);
-        }
-        for (int j = 0; j < n_kv; ++j) {
-          const int s = j % kStages, ph = ((j / kStages) & 1) ^ 1, key0 = j * BN;
-          if (!ptx::mbar_wait(&bars.k_empty[s], ph, abort_flag, p.err)) break;
-          ptx::mbar_arrive_expect_tx(&bars.k_full[s], 2 * kKChunk);
-          ptx::tma_load_4d(sm + kOffKn + s * kKChunk, &tm_kn, &bars.k_full[s], 0, h, key0, b);
-          ptx::tma_load_3d(sm + kOffKr + s * kKChunk, &tm_kr, &bars.k_full[s], 0, key0, b);
-          if (!ptx::mbar_wait(&bars.v8_empty[s], ph, abort_flag, p.err)) break;
-          ptx::mbar_arrive_expect_tx(&bars.v8_full[s], kKChunk);
-          ptx::tma_load_4d(sm + kOffV8 + s * kKChunk, &tm_v, &bars.v8_full[s], 0, h, key0, b);
-        }
+  if (warp == 0) {
+    // -------------------------------------------------------------- producer
+    if (ptx::elect_one()) {
+      ptx::mbar_arrive_expect_tx(&bars.q_full, 2 * kQChunk);
+      ptx::tma_load_4d(sm + kOffQn, &tm_qn, &bars.q_full, 0, h, q_row0, b);
+      ptx::tma_load_4d(sm + kOffQr, &tm_qr, &bars.q_full, 0, h, q_row0, b);
+      for (int j = 0; j < n_kv; ++j) {
+        const int s = j % kStages, ph = ((j / kStages) & 1) ^ 1, key0 = j * BN;
+        if (!ptx::mbar_wait(&bars.k_empty[s], ph, abort_flag, p.err)) break;
+        ptx::mbar_arrive_expect_tx(&bars.k_full[s], 2 * kKChunk);
+        ptx::tma_load_4d(sm + kOffKn + s * kKChunk, &tm_kn, &bars.k_full[s], 0, h, key0, b);
+        ptx::tma_load_3d(sm + kOffKr + s * kKChunk, &tm_kr, &bars.k_full[s], 0, key0, b);
+        if (!ptx::mbar_wait(&bars.v8_empty[s], ph, abort_flag, p.err)) break;
+        ptx::mbar_arrive_expect_tx(&bars.v8_full[s], kKChunk);
+        ptx::tma_load_4d(sm + kOffV8 + s * kKChunk, &tm_v, &bars.v8_full[s], 0, h, key0, b);
       }
-    } else if (warp == 1) {
-      // ------------------------------------------------------------ MMA issuer
-      if (ptx::elect_one()) {
-        constexpr uint32_t kIdS8 = ptx::make_idesc(0, BM, BN, 0, 0);   // e4m3 x e4m3
-        constexpr uint32_t kIdS16 = ptx::make_idesc(1, BM, BN, 0, 0);  // bf16 rope
-        constexpr uint32_t kIdPV = ptx::make_idesc(1, BM, 128, 0, 1);
-        const uint32_t qn = ptx::smem_u32(sm + kOffQn), qr = ptx::smem_u32(sm + kOffQr);
-        const uint32_t kn = ptx::smem_u32(sm + kOffKn), kr = ptx::smem_u32(sm + kOffKr);
-        const uint32_t vb = ptx::smem_u32(sm + kOffVb);
-        bool ok = ptx::mbar_wait(&bars.q_full, 0, abort_flag, p.err);
-        auto wait_k = [&](int j) {
-          return ptx::mbar_wait(&bars.k_full[j % kStages], (j / kStages) & 1, abort_flag, p.err);
-        };
-        auto issue_s = [&](int t, int j) {
-          const int s = j % kStages;
-          const uint32_t dn = tmem + t * 256, dr = dn + 64;
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------------- MMA issuer
+    if (ptx::elect_one()) {
+      constexpr uint32_t kIdS8 = ptx::make_idesc(0, BM, BN, 0, 0);   // e4m3 x e4m3
+      constexpr uint32_t kIdS16 = ptx::make_idesc(1, BM, BN, 0, 0);  // bf16 rope
+      constexpr uint32_t kIdPV = ptx::make_idesc(1, BM, 128, 0, 1);
+      const uint32_t qn = ptx::smem_u32(sm + kOffQn), qr = ptx::smem_u32(sm + kOffQr);
+      const uint32_t kn = ptx::smem_u32(sm + kOffKn), kr = ptx::smem_u32(sm + kOffKr);
+      const uint32_t vb = ptx::smem_u32(sm + kOffVb);
+      bool ok = ptx::mbar_wait(&bars.q_full, 0, abort_flag, p.err);
+      // S(j): both score buffers of tile parity j & 1, then the K slot is free
+      auto s_tile = [&](int j) -> bool {
+        const int s = j % kStages;
+        if (!ptx::mbar_wait(&bars.k_full[s], (j / kStages) & 1, abort_flag, p.err)) return false;
+        ptx::tc_fence_after();
+        const uint32_t dn = tmem + (j & 1) * 64, dr = tmem + 128 + (j & 1) * 64;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {  // nope: K = 128 fp8 = 4 x 32
-            const uint64_t da = ptx::sw128_desc(qn + t * kQChunk + k * 32, 16, 1024);
-            const uint64_t db = ptx::sw128_desc(kn + s * kKChunk + k * 32, 16, 1024);
-            ptx::mma_f8_ss(dn, da, db, kIdS8, k > 0);
-          }
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {  // rope: K = 64 bf16 = 4 x 16
-            const uint64_t da = ptx::sw128_desc(qr + t * kQChunk + k * 32, 16, 1024);
-            const uint64_t db = ptx::sw128_desc(kr + s * kKChunk + k * 32, 16, 1024);
-            ptx::mma_bf16_ss(dr, da, db, kIdS16, k > 0);
-          }
-        };
-        auto issue_pv = [&](int t, int j) {
-          const uint32_t v = vb + (j % kStages) * 2 * kKChunk;
-          const uint32_t d = tmem + t * 256 + 128;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {  // high part of P': columns 0..31
-            const uint64_t db = ptx::sw128_desc(v + k * 2048, kKChunk, 1024);
-            ptx::mma_bf16_ts(d, tmem + t * 256 + k * 8, db, kIdPV, (j > 0 || k > 0) ? 1u : 0u);
-          }
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {  // low part of P': columns 32..63
-            const uint64_t db = ptx::sw128_desc(v + k * 2048, kKChunk, 1024);
-            ptx::mma_bf16_ts(d, tmem + t * 256 + 32 + k * 8, db, kIdPV, 1u);
-          }
-        };
-        if (ok && n_kv > 0 && (ok = wait_k(0))) {
-          ptx::tc_fence_after();
-          issue_s(0, 0);
-          ptx::mma_commit(&bars.s_full[0]);
-          issue_s(1, 0);
-          ptx::mma_commit(&bars.s_full[1]);
-          ptx::mma_commit(&bars.k_empty[0]);
+        for (int k = 0; k < 4; ++k) {  // nope: K = 128 fp8 = 4 x 32
+          const uint64_t da = ptx::sw128_desc(qn + k * 32, 16, 1024);
+          const uint64_t db = ptx::sw128_desc(kn + s * kKChunk + k * 32, 16, 1024);
+          ptx::mma_f8_ss(dn, da, db, kIdS8, k > 0);
         }
-        for (int j = 0; ok && j < n_kv; ++j) {
-          const int s = j % kStages;
-          const bool more = j + 1 < n_kv;
-          bool k_ready = false;
-          if (!(ok = ptx::mbar_wait(&bars.vb_full[s], (j / kStages) & 1, abort_flag, p.err))) break;
-          if (j < n_kv0) {
-            if (!(ok = ptx::mbar_wait(&bars.p_full[0], j & 1, abort_flag, p.err))) break;
-            ptx::tc_fence_after();
-            issue_pv(0, j);
-            ptx::mma_commit(&bars.o_done[0]);
-            if (j + 1 < n_kv0) {
-              if (!(ok = wait_k(j + 1))) break;
-              k_ready = true;
-              ptx::tc_fence_after();
-              issue_s(0, j + 1);
-              ptx::mma_commit(&bars.s_full[0]);
-            }
-          }
-          if (!(ok = ptx::mbar_wait(&bars.p_full[1], j & 1, abort_flag, p.err))) break;
-          ptx::tc_fence_after();
-          issue_pv(1, j);
-          ptx::mma_commit(&bars.o_done[1]);
-          ptx::mma_commit(&bars.vb_empty[s]);
-          if (more) {
-            if (!k_ready && !(ok = wait_k(j + 1))) break;
-            ptx::tc_fence_after();
-            issue_s(1, j + 1);
-            ptx::mma_commit(&bars.s_full[1]);
-            ptx::mma_commit(&bars.k_empty[(j + 1) % kStages]);
-          }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {  // rope: K = 64 bf16 = 4 x 16
+          const uint64_t da = ptx::sw128_desc(qr + k * 32, 16, 1024);
+          const uint64_t db = ptx::sw128_desc(kr + s * kKChunk + k * 32, 16, 1024);
+          ptx::mma_bf16_ss(dr, da, db, kIdS16, k > 0);
         }
-      }
-    } else {
-      // ------------------------------------------------------------ converters (64 threads)
-      const int ct = threadIdx.x - 64;  // one key row each
-      bool ok = true;
+        ptx::mma_commit(&bars.s_full[j & 1]);
+        ptx::mma_commit(&bars.k_empty[s]);
+        return true;
+      };
+      // O += P'(j) V(j): key block k (16 keys) belongs to warpgroup k / 2, whose P' high
+      // and low halves sit at columns (k / 2) * 32 + (k & 1) * 8 and 16 further on
+      auto pv_tile = [&](int j) {
+        const uint32_t v = vb + (j % kStages) * 2 * kKChunk;
+        const uint32_t pa = tmem + (j & 1) * 64;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint64_t db = ptx::sw128_desc(v + k * 2048, kKChunk, 1024);
+          const uint32_t hi = pa + (k >> 1) * 32 + (k & 1) * 8;
+          ptx::mma_bf16_ts(tmem + 256, hi, db, kIdPV, (j > 0 || k > 0) ? 1u : 0u);
+          ptx::mma_bf16_ts(tmem + 256, hi + 16, db, kIdPV, 1u);
+        }
+      };
+      if (ok && n_kv > 0) ok = s_tile(0);
+      if (ok && n_kv > 1) ok = s_tile(1);
       for (int j = 0; ok && j < n_kv; ++j) {
-        const int s = j % kStages, ph = (j / kStages) & 1, key = j * BN + ct;
-        // slot s is free once PV(j - kStages) is done (which needed that tile's softmax)
-        ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.vb_empty[s], ph ^ 1, abort_flag, p.err));
-        if (!ok) break;
-        bars.ks[s][ct] = key < p.S ? __ldg(p.k_scale + (size_t)b * p.S + key) : 0.f;
-        ptx::mbar_arrive(&bars.ks_full[s]);
-        // V8 (64 keys x 128 fp8, one swizzled 128-byte row per key) -> bf16 N-major tile
-        ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.v8_full[s], ph, abort_flag, p.err));
-        if (!ok) break;
-        const unsigned char* src = sm + kOffV8 + s * kKChunk + ct * 128;
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {  // 16 fp8 values = logical 16-byte group g of the row
-          const uint4 raw = *reinterpret_cast<const uint4*>(src + ((g ^ (ct & 7)) << 4));
-          const uint8_t* by = reinterpret_cast<const uint8_t*>(&raw);
-          uint32_t w[8];
-#pragma unroll
-          for (int x = 0; x < 8; ++x)
-            w[x] = ptx::pack_bf16x2(e4m3_to_f32(by[2 * x]), e4m3_to_f32(by[2 * x + 1]));
-          // columns 16g .. 16g+15 -> chunk (g / 4), logical groups 2(g%4) and 2(g%4)+1
-          unsigned char* dst = sm + kOffVb + s * 2 * kKChunk + (g >> 2) * kKChunk + ct * 128;
-          const int g0 = 2 * (g & 3);
-          *reinterpret_cast<uint4*>(dst + ((g0 ^ (ct & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-          *reinterpret_cast<uint4*>(dst + (((g0 + 1) ^ (ct & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
-        }
-        ptx::fence_proxy_async();
-        ptx::mbar_arrive(&bars.v8_empty[s]);
-        ptx::mbar_arrive(&bars.vb_full[s]);
+        const int s = j % kStages;
+        if (!(ok = ptx::mbar_wait(&bars.vb_full[s], (j / kStages) & 1, abort_flag, p.err))) break;
+        if (!(ok = ptx::mbar_wait(&bars.p_full[j & 1], (j >> 1) & 1, abort_flag, p.err))) break;
+        ptx::tc_fence_after();
+        pv_tile(j);
+        ptx::mma_commit(&bars.o_done);
+        ptx::mma_commit(&bars.vb_empty[s]);
+        // the score buffers of parity j & 1 are free once PV(j) has read P'(j) (in order)
+        if (j + 2 < n_kv) ok = s_tile(j + 2);
       }
+    }
+  } else if (warp < 4 || warp >= 12) {
+    // -------------------------------------------------------------- converters (128 threads)
+    const int ct = warp < 4 ? threadIdx.x - 64 : threadIdx.x - 320;  // 0..127
+    const int row = ct & (BN - 1), g_first = (ct >> 6) * 4;  // key row, first of 4 groups
+    bool ok = true;
+    for (int j = 0; ok && j < n_kv; ++j) {
+      const int s = j % kStages, ph = (j / kStages) & 1, key = j * BN + ct;
+      // slot s is free once PV(j - kStages) is done (which needed that tile's softmax)
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.vb_empty[s], ph ^ 1, abort_flag, p.err));
+      if (!ok) break;
+      if (ct < BN) bars.ks[s][ct] = key < p.S ? __ldg(p.k_scale + (size_t)b * p.S + key) : 0.f;
+      ptx::mbar_arrive(&bars.ks_full[s]);
+      // V8 (64 keys x 128 fp8, one swizzled 128-byte row per key) -> bf16 N-major tile
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.v8_full[s], ph, abort_flag, p.err));
+      if (!ok) break;
+      const unsigned char* src = sm + kOffV8 + s * kKChunk + row * 128;
+#pragma unroll
+      for (int g = g_first; g < g_first + 4; ++g) {  // 16 fp8 values = 16-byte group g of the row
+        const uint4 raw = *reinterpret_cast<const uint4*>(src + ((g ^ (row & 7)) << 4));
+        const uint8_t* by = reinterpret_cast<const uint8_t*>(&raw);
+        uint32_t w[8];
+#pragma unroll
+        for (int x = 0; x < 8; ++x)
+          w[x] = ptx::pack_bf16x2(e4m3_to_f32(by[2 * x]), e4m3_to_f32(by[2 * x + 1]));
+        // columns 16g .. 16g+15 -> chunk (g / 4), logical groups 2(g%4) and 2(g%4)+1
+        unsigned char* dst = sm + kOffVb + s * 2 * kKChunk + (g >> 2) * kKChunk + row * 128;
+        const int g0 = 2 * (g & 3);
+        *reinterpret_cast<uint4*>(dst + ((g0 ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(dst + (((g0 + 1) ^ (row & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+      ptx::fence_proxy_async();
+      ptx::mbar_arrive(&bars.v8_empty[s]);
+      ptx::mbar_arrive(&bars.vb_full[s]);
     }
   } else {
     // -------------------------------------------------------------- softmax warpgroups
-    ptx::regs_inc<224>();
-    const int t = (warp >> 2) - 1;
-    const int r = (warp & 3) * 32 + lane;
-    const int i = q_row0 + t * BM + r;
+    const int w = (warp >> 2) - 1;          // 0: keys 0..31 of a tile, 1: keys 32..63
+    const int r = (warp & 3) * 32 + lane;   // query row == TMEM lane
+    const int i = q_row0 + r;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t sn_addr = tmem + lane_off + t * 256;
-    const uint32_t o_addr = sn_addr + 128;
+    const uint32_t o_addr = tmem + lane_off + 256 + w * 64;  // this warpgroup's half of O
     const float qs = i < p.S ? __ldg(p.q_scale + (size_t)b * p.S + i) : 1.f;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    const int n_t = t == 0 ? n_kv0 : n_kv;  // key tiles this Q tile sees
-    for (int j = 0; j < n_t; ++j) {
-      ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.s_full[t], j & 1, abort_flag, p.err));
+    for (int j = 0; j < n_kv; ++j) {
+      const int buf = j & 1;
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.s_full[buf], (j >> 1) & 1, abort_flag, p.err));
       if (!ok) break;
       ptx::tc_fence_after();
       ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.ks_full[j % kStages], (j / kStages) & 1, abort_flag, p.err));
       if (!ok) break;
-      const float* ks = bars.ks[j % kStages];
-      float s[64];
+      const float* ks = bars.ks[j % kStages] + w * KH;
+      const uint32_t sn_addr = tmem + lane_off + buf * 64 + w * KH;
+      float s[KH];
       {
         uint32_t vn[32], vr[32];
+        ptx::tmem_ld32(sn_addr, vn);
+        ptx::tmem_ld32(sn_addr + 128, vr);
+        ptx::tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          ptx::tmem_ld32(sn_addr + c * 32, vn);
-          ptx::tmem_ld32(sn_addr + 64 + c * 32, vr);
-          ptx::tmem_ld_wait();
-#pragma unroll
-          for (int x = 0; x < 32; ++x)
-            s[c * 32 + x] = fmaf(__uint_as_float(vn[x]), qs * ks[c * 32 + x], __uint_as_float(vr[x])) *
-                            p.scale_log2;
-        }
+        for (int x = 0; x < KH; ++x)
+          s[x] = fmaf(__uint_as_float(vn[x]), qs * ks[x], __uint_as_float(vr[x])) * p.scale_log2;
       }
-      const int key0 = j * BN;
-      const bool need_mask = (key0 + BN > p.S) || (p.causal && key0 + BN - 1 > q_row0 + t * BM);
-      if (need_mask) {
+      const int key0 = j * BN + w * KH;
+      if ((key0 + KH > p.S) || (p.causal && key0 + KH - 1 > q_row0)) {
         const int lim = p.causal ? min(i + 1, p.S) : p.S;
 #pragma unroll
-        for (int x = 0; x < 64; ++x)
+        for (int x = 0; x < KH; ++x)
           if (key0 + x >= lim) s[x] = -INFINITY;
       }
-      float mx8[8];
+      float mx4[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-      for (int q = 0; q < 8; ++q) mx8[q] = s[q];
-#pragma unroll
-      for (int x = 8; x < 64; ++x) mx8[x & 7] = fmaxf(mx8[x & 7], s[x]);
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      for (int x = 4; x < KH; ++x) mx4[x & 3] = fmaxf(mx4[x & 3], s[x]);
+      // both warpgroups' partial maxima of the row -> the same tile maximum in each
+      bars.mx_part[buf][w][r] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&bars.mx_bar[buf]);
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.mx_bar[buf], (j >> 1) & 1, abort_flag, p.err));
+      if (!ok) break;
+      const float mx = fmaxf(bars.mx_part[buf][0][r], bars.mx_part[buf][1][r]);
       float m_use = m;
       if (j == 0) {
         m_use = mx;
       } else {
         const bool grow = mx > m + 8.0f;
         if (__any_sync(0xffffffffu, grow)) {
-          ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.o_done[t], (j - 1) & 1, abort_flag, p.err));
+          ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.o_done, (j - 1) & 1, abort_flag, p.err));
           if (!ok) break;
           ptx::tc_fence_after();
           const float alpha = grow ? ptx::ex2(m - mx) : 1.f;
           if (grow) m_use = mx;
           uint32_t v[32];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 2; ++c) {
             ptx::tmem_ld32(o_addr + c * 32, v);
             ptx::tmem_ld_wait();
 #pragma unroll
@@ -325,32 +299,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       m = m_use;
       const float neg_m = (m == -INFINITY) ? 0.f : -m;
       float ps[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t hi[32], lo[32];
+      uint32_t pk[32];  // P' high part (columns 0..15), low part (16..31)
 #pragma unroll
-      for (int x = 0; x < 32; ++x) {
+      for (int x = 0; x < KH / 2; ++x) {
         const float p0 = ptx::ex2(s[2 * x] + neg_m);
         const float p1 = ptx::ex2(s[2 * x + 1] + neg_m);
         ps[x & 3] += p0 + p1;
         const float a = p0 * ks[2 * x], bq = p1 * ks[2 * x + 1];
         const uint32_t hw = ptx::pack_bf16x2(a, bq);
-        hi[x] = hw;
-        lo[x] = ptx::pack_bf16x2(a - __uint_as_float(hw << 16), bq - __uint_as_float(hw & 0xffff0000u));
+        pk[x] = hw;
+        pk[16 + x] = ptx::pack_bf16x2(a - __uint_as_float(hw << 16), bq - __uint_as_float(hw & 0xffff0000u));
       }
-      ptx::tmem_st32(sn_addr, hi);       // P' high part: columns 0..31
-      ptx::tmem_st32(sn_addr + 32, lo);  // P' low part: columns 32..63
+      ptx::tmem_st32(sn_addr, pk);
       l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(&bars.p_full[t]);
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&bars.p_full[buf]);
     }
-    if (ok && n_t > 0 &&
-        __all_sync(0xffffffffu, ptx::mbar_wait(&bars.o_done[t], (n_t - 1) & 1, abort_flag, p.err))) {
+    if (ok && n_kv > 0) {
+      // the row sum is the sum of both warpgroups' partial sums (in the same order in both)
+      bars.l_part[w][r] = l;
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&bars.l_bar);
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.l_bar, 0, abort_flag, p.err)) &&
+           __all_sync(0xffffffffu, ptx::mbar_wait(&bars.o_done, (n_kv - 1) & 1, abort_flag, p.err));
+    }
+    if (ok && n_kv > 0) {
       ptx::tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float lt = bars.l_part[0][r] + bars.l_part[1][r];
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
       const bool store = i < p.S;
-      const size_t row_off = ((static_cast<size_t>(b) * p.S + i) * p.H + h) * 128;
+      const size_t row_off = ((static_cast<size_t>(b) * p.S + i) * p.H + h) * 128 + w * 64;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t v[32];
         ptx::tmem_ld32(o_addr + c * 32, v);
         ptx::tmem_ld_wait();
@@ -365,19 +347,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + row_off + c * 32);
 #pragma unroll
             for (int x = 0; x < 4; ++x) {
-              uint4 w;
-              w.x = ptx::pack_bf16x2(__uint_as_float(v[8 * x + 0]) * inv, __uint_as_float(v[8 * x + 1]) * inv);
-              w.y = ptx::pack_bf16x2(__uint_as_float(v[8 * x + 2]) * inv, __uint_as_float(v[8 * x + 3]) * inv);
-              w.z = ptx::pack_bf16x2(__uint_as_float(v[8 * x + 4]) * inv, __uint_as_float(v[8 * x + 5]) * inv);
-              w.w = ptx::pack_bf16x2(__uint_as_float(v[8 * x + 6]) * inv, __uint_as_float(v[8 * x + 7]) * inv);
-              dst[x] = w;
+              uint4 wv;
+              wv.x = ptx::pack_bf16x2(__uint_as_float(v[8 * x + 0]) * inv, __uint_as_float(v[8 * x + 1]) * inv);
+              wv.y = ptx::pack_bf16x2(__uint_as_float(v[8 * x + 2]) * inv, __uint_as_float(v[8 * x + 3]) * inv);
+              wv.z = ptx::pack_bf16x2(__uint_as_float(v[8 * x + 4]) * inv, __uint_as_float(v[8 * x + 5]) * inv);
+              wv.w = ptx::pack_bf16x2(__uint_as_float(v[8 * x + 6]) * inv, __uint_as_float(v[8 * x + 7]) * inv);
+              dst[x] = wv;
             }
           }
         }
       }
-      if (store)
+      if (store && w == 0)
         p.lse[(static_cast<size_t>(b) * p.H + h) * p.S + i] =
-            l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+            lt > 0.f ? (m + __log2f(lt)) * 0.69314718055994531f : -INFINITY;
     }
   }
   ptx::tc_fence_before();
@@ -425,7 +407,7 @@ cudaError_t launch_prefill_sm103_fp8(const void* q_nope, const void* q_rope, con
   p.H = H;
   p.S = S;
   p.causal = causal;
-  p.nrb = (S + NQ * BM - 1) / (NQ * BM);
+  p.nrb = (S + BM - 1) / BM;
   p.out_f32 = out_f32 ? 1 : 0;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   p.q_scale = q_scale;
@@ -435,9 +417,6 @@ cudaError_t launch_prefill_sm103_fp8(const void* q_nope, const void* q_rope, con
   p.err = err;
   static bool ready = false;
   if (!ready) {
-    cudaFuncAttributes fa;
-    if ((e = cudaFuncGetAttributes(&fa, prefill_fp8_kernel)) != cudaSuccess) return e;
-    if (fa.numRegs != 168) return cudaErrorInvalidDeviceFunction;  // setmaxnreg split
     if ((e = cudaFuncSetAttribute(prefill_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   kSmemAlloc)) != cudaSuccess)
       return e;
