@@ -263,14 +263,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int x = 0; x < 128; ++x)
           if (key0 + x >= lim) s[x] = -INFINITY;
       }
-      // row max as 8 independent chains (few warps per scheduler: latency is not hidden)
-      float mx8[8];
+      // row max: four independent chains of three-input maxima
+      float mx4[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-      for (int q = 0; q < 8; ++q) mx8[q] = s[q];
-#pragma unroll
-      for (int x = 8; x < 128; ++x) mx8[x & 7] = fmaxf(mx8[x & 7], s[x]);
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      for (int x = 4; x < 128; x += 2) mx4[(x >> 1) & 3] = ptx::fmax3(mx4[(x >> 1) & 3], s[x], s[x + 1]);
+      const float mx = ptx::fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]);
       const float m_tile = mx * p.scale_log2;  // -inf stays -inf
       float m_use = m;
       if (j == 0) {
@@ -304,30 +301,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       m = m_use;
       const float neg_m = -m;
-      float ps[4] = {0.f, 0.f, 0.f, 0.f}, pr[4] = {0.f, 0.f, 0.f, 0.f};
+      // two keys per packed fp32x2 instruction: exponent argument, exact row sum and the
+      // sum of the bf16-rounded values the PV product uses (O is normalised by the latter,
+      // so a dominant key is normalised exactly; the LSE uses the exact sum)
+      const uint64_t sc2 = ptx::f2(p.scale_log2, p.scale_log2), nm2 = ptx::f2(neg_m, neg_m);
+      uint64_t ps2[2] = {ptx::f2(0.f, 0.f), ptx::f2(0.f, 0.f)};
+      uint64_t pr2[2] = {ptx::f2(0.f, 0.f), ptx::f2(0.f, 0.f)};
       uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
 #pragma unroll
         for (int x = 0; x < 32; ++x) {
-          const float a0 = fmaf(s[c * 64 + 2 * x], p.scale_log2, neg_m);
-          const float a1 = fmaf(s[c * 64 + 2 * x + 1], p.scale_log2, neg_m);
-          const float p0 = ptx::ex2(a0);
-          const float p1 = ptx::ex2(a1);
-          // O is normalised by the sum of the bf16-rounded values the PV product uses (so a
-          // dominant key is normalised exactly); the LSE uses the exact sum
+          const uint64_t a2 = ptx::fma2(ptx::f2(s[c * 64 + 2 * x], s[c * 64 + 2 * x + 1]), sc2, nm2);
+          const float p0 = ptx::ex2(ptx::f2_lo(a2));
+          const float p1 = ptx::ex2(ptx::f2_hi(a2));
           const uint32_t w = ptx::pack_bf16x2(p0, p1);
           pk[x] = w;
-          ps[x & 3] += p0 + p1;
-          pr[x & 3] += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+          ps2[x & 1] = ptx::add2(ps2[x & 1], ptx::f2(p0, p1));
+          pr2[x & 1] = ptx::add2(pr2[x & 1], ptx::f2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)));
         }
         ptx::tmem_st32(s_addr + c * 32, pk);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         ptx::mbar_arrive(&bars.p_full[t][c]);
       }
-      l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-      lr += (pr[0] + pr[1]) + (pr[2] + pr[3]);
+      const uint64_t ps_all = ptx::add2(ps2[0], ps2[1]), pr_all = ptx::add2(pr2[0], pr2[1]);
+      l += ptx::f2_lo(ps_all) + ptx::f2_hi(ps_all);
+      lr += ptx::f2_lo(pr_all) + ptx::f2_hi(pr_all);
     }
     // epilogue: O / l -> out, LSE
     if (ok && n_t > 0 &&
