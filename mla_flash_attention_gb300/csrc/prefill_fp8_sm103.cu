@@ -246,28 +246,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       const float* ks = bars.ks[j % kStages] + w * KH;
       const uint32_t sn_addr = tmem + lane_off + buf * 64 + w * KH;
-      float s[KH];
+      // unscaled scores qs ks_x Sn + Sr, two keys per packed fp32x2 instruction (the softmax
+      // scale is applied inside the exponent argument)
+      uint64_t s2[KH / 2];
       {
         uint32_t vn[32], vr[32];
         ptx::tmem_ld32(sn_addr, vn);
         ptx::tmem_ld32(sn_addr + 128, vr);
         ptx::tmem_ld_wait();
+        const uint64_t qs2 = ptx::f2(qs, qs);
 #pragma unroll
-        for (int x = 0; x < KH; ++x)
-          s[x] = fmaf(__uint_as_float(vn[x]), qs * ks[x], __uint_as_float(vr[x])) * p.scale_log2;
+        for (int x = 0; x < KH / 2; ++x)
+          s2[x] = ptx::fma2(ptx::f2(__uint_as_float(vn[2 * x]), __uint_as_float(vn[2 * x + 1])),
+                            ptx::mul2(qs2, ptx::f2(ks[2 * x], ks[2 * x + 1])),
+                            ptx::f2(__uint_as_float(vr[2 * x]), __uint_as_float(vr[2 * x + 1])));
       }
       const int key0 = j * BN + w * KH;
       if ((key0 + KH > p.S) || (p.causal && key0 + KH - 1 > q_row0)) {
         const int lim = p.causal ? min(i + 1, p.S) : p.S;
 #pragma unroll
-        for (int x = 0; x < KH; ++x)
-          if (key0 + x >= lim) s[x] = -INFINITY;
+        for (int x = 0; x < KH / 2; ++x)
+          s2[x] = ptx::f2(key0 + 2 * x >= lim ? -INFINITY : ptx::f2_lo(s2[x]),
+                          key0 + 2 * x + 1 >= lim ? -INFINITY : ptx::f2_hi(s2[x]));
       }
-      float mx4[4] = {s[0], s[1], s[2], s[3]};
+      float mx4[4] = {ptx::f2_lo(s2[0]), ptx::f2_hi(s2[0]), ptx::f2_lo(s2[1]), ptx::f2_hi(s2[1])};
 #pragma unroll
-      for (int x = 4; x < KH; ++x) mx4[x & 3] = fmaxf(mx4[x & 3], s[x]);
-      // both warpgroups' partial maxima of the row -> the same tile maximum in each
-      bars.mx_part[buf][w][r] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      for (int x = 2; x < KH / 2; ++x) mx4[x & 3] = ptx::fmax3(mx4[x & 3], ptx::f2_lo(s2[x]), ptx::f2_hi(s2[x]));
+      // both warpgroups' partial maxima of the row -> the same tile maximum in each (scaled
+      // to the exponent domain; the scale is positive, -inf stays -inf)
+      bars.mx_part[buf][w][r] = ptx::fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]) * p.scale_log2;
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&bars.mx_bar[buf]);
       ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.mx_bar[buf], (j >> 1) & 1, abort_flag, p.err));
@@ -298,20 +305,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       m = m_use;
       const float neg_m = (m == -INFINITY) ? 0.f : -m;
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint64_t sc2 = ptx::f2(p.scale_log2, p.scale_log2), nm2 = ptx::f2(neg_m, neg_m);
+      uint64_t ps2[2] = {ptx::f2(0.f, 0.f), ptx::f2(0.f, 0.f)};
       uint32_t pk[32];  // P' high part (columns 0..15), low part (16..31)
 #pragma unroll
       for (int x = 0; x < KH / 2; ++x) {
-        const float p0 = ptx::ex2(s[2 * x] + neg_m);
-        const float p1 = ptx::ex2(s[2 * x + 1] + neg_m);
-        ps[x & 3] += p0 + p1;
-        const float a = p0 * ks[2 * x], bq = p1 * ks[2 * x + 1];
-        const uint32_t hw = ptx::pack_bf16x2(a, bq);
+        const uint64_t a2 = ptx::fma2(s2[x], sc2, nm2);
+        const float p0 = ptx::ex2(ptx::f2_lo(a2));
+        const float p1 = ptx::ex2(ptx::f2_hi(a2));
+        const uint64_t pp = ptx::f2(p0, p1);
+        ps2[x & 1] = ptx::add2(ps2[x & 1], pp);
+        const uint64_t ab = ptx::mul2(pp, ptx::f2(ks[2 * x], ks[2 * x + 1]));  // P' = p ks
+        const uint32_t hw = ptx::pack_bf16x2(ptx::f2_lo(ab), ptx::f2_hi(ab));
         pk[x] = hw;
-        pk[16 + x] = ptx::pack_bf16x2(a - __uint_as_float(hw << 16), bq - __uint_as_float(hw & 0xffff0000u));
+        const uint64_t lo2 = ptx::sub2(ab, ptx::f2(__uint_as_float(hw << 16), __uint_as_float(hw & 0xffff0000u)));
+        pk[16 + x] = ptx::pack_bf16x2(ptx::f2_lo(lo2), ptx::f2_hi(lo2));
       }
       ptx::tmem_st32(sn_addr, pk);
-      l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+      const uint64_t ps_all = ptx::add2(ps2[0], ps2[1]);
+      l += ptx::f2_lo(ps_all) + ptx::f2_hi(ps_all);
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       __syncwarp();
