@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // so a dominant key is normalised exactly; the LSE uses the exact sum)
       const uint64_t sc2 = ptx::f2(p.scale_log2, p.scale_log2), nm2 = ptx::f2(neg_m, neg_m);
       uint64_t ps2[2] = {ptx::f2(0.f, 0.f), ptx::f2(0.f, 0.f)};
-      uint64_t pr2[2] = {ptx::f2(0.f, 0.f), ptx::f2(0.f, 0.f)};
+      float pr[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
@@ -318,16 +318,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t w = ptx::pack_bf16x2(p0, p1);
           pk[x] = w;
           ps2[x & 1] = ptx::add2(ps2[x & 1], ptx::f2(p0, p1));
-          pr2[x & 1] = ptx::add2(pr2[x & 1], ptx::f2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)));
+          ptx::add_bf16x2(pr[2 * (x & 1)], pr[2 * (x & 1) + 1], w);
         }
         ptx::tmem_st32(s_addr + c * 32, pk);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         ptx::mbar_arrive(&bars.p_full[t][c]);
       }
-      const uint64_t ps_all = ptx::add2(ps2[0], ps2[1]), pr_all = ptx::add2(pr2[0], pr2[1]);
+      const uint64_t ps_all = ptx::add2(ps2[0], ps2[1]);
       l += ptx::f2_lo(ps_all) + ptx::f2_hi(ps_all);
-      lr += ptx::f2_lo(pr_all) + ptx::f2_hi(pr_all);
+      lr += (pr[0] + pr[1]) + (pr[2] + pr[3]);
     }
     // epilogue: O / l -> out, LSE
     if (ok && n_t > 0 &&

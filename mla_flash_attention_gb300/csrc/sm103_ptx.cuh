@@ -350,6 +350,13 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+// acc_lo += bf16 low half of w, acc_hi += bf16 high half (the bf16 operand widens exactly)
+__device__ __forceinline__ void add_bf16x2(float& acc_lo, float& acc_hi, uint32_t w) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(acc_lo), "+f"(acc_hi)
+      : "r"(w));
+}
 // max of three (one instruction)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
