@@ -18,12 +18,6 @@ __device__ __forceinline__ float bf16_to_f32(uint16_t bits) {
   return __uint_as_float(static_cast<uint32_t>(bits) << 16);
 }
 
-__device__ __forceinline__ float e4m3_to_f32(uint8_t code) {
-  __nv_fp8_e4m3 v;
-  v.__x = code;
-  return static_cast<float>(v);
-}
-
 __device__ __forceinline__ uint16_t f32_to_bf16_rne(float x) {
   __nv_bfloat16 h = __float2bfloat16_rn(x);
   return *reinterpret_cast<uint16_t*>(&h);

@@ -427,15 +427,14 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
             ptx::mbar_arrive(&bars.conv_sync);
             ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.conv_sync, (3 * g + k) & 1, abort_flag, p.err));
             if (!ok) break;
-            const uint8_t* bytes = reinterpret_cast<const uint8_t*>(raw);
+            const uint32_t* words = reinterpret_cast<const uint32_t*>(raw);
             unsigned char* dst = st + c * kPageChunk + row * 128;
 #pragma unroll
             for (int gr = 0; gr < 8; ++gr) {
               uint32_t w[4];
 #pragma unroll
               for (int x = 0; x < 4; ++x)
-                w[x] = ptx::pack_bf16x2(e4m3_to_f32(bytes[gr * 8 + 2 * x]),
-                                        e4m3_to_f32(bytes[gr * 8 + 2 * x + 1]));
+                w[x] = ptx::e4m3x2_to_bf16x2(words[gr * 2 + (x >> 1)] >> (16 * (x & 1)));
               *reinterpret_cast<uint4*>(dst + ((gr ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
           }

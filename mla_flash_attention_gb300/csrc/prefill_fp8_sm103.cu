@@ -212,11 +212,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int g = g_first; g < g_first + 4; ++g) {  // 16 fp8 values = 16-byte group g of the row
         const uint4 raw = *reinterpret_cast<const uint4*>(src + ((g ^ (row & 7)) << 4));
-        const uint8_t* by = reinterpret_cast<const uint8_t*>(&raw);
+        const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
         uint32_t w[8];
 #pragma unroll
-        for (int x = 0; x < 8; ++x)
-          w[x] = ptx::pack_bf16x2(e4m3_to_f32(by[2 * x]), e4m3_to_f32(by[2 * x + 1]));
+        for (int x = 0; x < 4; ++x) {
+          w[2 * x] = ptx::e4m3x2_to_bf16x2(rw[x]);
+          w[2 * x + 1] = ptx::e4m3x2_to_bf16x2(rw[x] >> 16);
+        }
         // columns 16g .. 16g+15 -> chunk (g / 4), logical groups 2(g%4) and 2(g%4)+1
         unsigned char* dst = sm + kOffVb + s * 2 * kKChunk + (g >> 2) * kKChunk + row * 128;
         const int g0 = 2 * (g & 3);

@@ -357,6 +357,22 @@ __device__ __forceinline__ void add_bf16x2(float& acc_lo, float& acc_hi, uint32_
       : "+f"(acc_lo), "+f"(acc_hi)
       : "r"(w));
 }
+// Two e4m3 codes (low byte = first) -> packed bf16x2, exactly: the pair is widened to f16
+// in one instruction (every e4m3 value is an f16 normal or zero), then to fp32 and bf16.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t codes16) {
+  float lo, hi;
+  asm("{\n\t.reg .b16 c, l, h;\n\t.reg .b32 f;\n\t"
+      "cvt.u16.u32 c, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 f, c;\n\t"
+      "mov.b32 {l, h}, f;\n\t"
+      "cvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(codes16));
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // max of three (one instruction)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
