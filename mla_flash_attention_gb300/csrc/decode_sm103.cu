@@ -70,7 +70,9 @@ struct Plan {
 };
 
 struct Bars {
-  uint64_t stage_full[kStages], stage_ready[kStages], stage_empty[kStages];
+  // stage_ready[s][k]: bf16 pages are ready at once (k = 0); fp8 pages in three parts, k = 0..2
+  // covering 64-column chunks 3k..3k+2, as the in-place widening completes them
+  uint64_t stage_full[kStages], stage_ready[kStages][3], stage_empty[kStages];
   uint64_t s_full[2], p_full[2], o_done, conv_sync;
   uint64_t q_free, q_lo_full, q_cp_done, q_hi_full;  // per-sequence Q staging
   uint32_t tmem_base;
@@ -199,6 +201,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   __shared__ Bars bars;
   constexpr int kThreads = kThreadsOf<kFp8>, kPrepThreads = kPrepOf<kFp8>;
+  constexpr int kParts = kFp8 ? 3 : 1;  // readiness parts of a page stage
   const int warp = threadIdx.x >> 5;
   const int unit = blockIdx.x >> 1, half = blockIdx.x & 1;
   const int TH = p.T * p.H;
@@ -207,7 +210,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
     bars.abort_flag = 0;
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&bars.stage_full[s], 1);
-      ptx::mbar_init(&bars.stage_ready[s], kPrepThreads);
+      for (int k = 0; k < 3; ++k) ptx::mbar_init(&bars.stage_ready[s][k], kPrepThreads);
       ptx::mbar_init(&bars.stage_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -295,16 +298,19 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
       const uint32_t o_tm = tmem + 256;
       int g = 0, nseg = 0;
       bool ok = true;
-      auto issue_s = [&](int gg) {
+      // part `part` of S(gg): all 36 k-steps (bf16), or k-steps 12 part .. 12 part + 11 (fp8)
+      auto issue_s = [&](int gg, int part) {
         const uint32_t st = stage0 + (gg % kStages) * kStageBytes;
         const uint32_t d = tmem + 128 + (gg & 1) * 64;
 #pragma unroll
         for (int k = 0; k < 16; ++k) {  // latent 0..255: A from TMEM
+          if (kFp8 && k / 12 != part) continue;
           const uint64_t db = ptx::sw128_desc(st + (k >> 2) * kPageChunk + (k & 3) * 32, 16, 1024);
           ptx::mma_bf16_ts(d, tmem + k * 8, db, kIdS, k > 0);
         }
 #pragma unroll
         for (int k = 16; k < 36; ++k) {  // latent 256..511 + rope: A from shared memory
+          if (kFp8 && k / 12 != part) continue;
           const int kq = k - 16;
           const uint64_t da = ptx::sw128_desc(qhi + (kq >> 2) * kQChunk + (kq & 3) * 32, 16, 1024);
           const uint64_t db = ptx::sw128_desc(st + (k >> 2) * kPageChunk + (k & 3) * 32, 16, 1024);
@@ -342,17 +348,23 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
         ptx::tc_fence_after();
         const int g_end = g + (hi - lo), g_first = g;
         int gs = g, gp = g;  // next page whose S / whose PV is to be issued
+        int sp = 0;          // next part of S(gs)
         long long t0 = clock64();
         while (gp < g_end) {
           bool progress = false;
           // S(gs) may run at most one page ahead of the oldest unissued PV (two S buffers)
           if (gs < g_end && gs <= gp + 1 &&
-              ptx::mbar_test_wait(&bars.stage_ready[gs % kStages], (gs / kStages) & 1)) {
+              ptx::mbar_test_wait(&bars.stage_ready[gs % kStages][sp], (gs / kStages) & 1)) {
             ptx::tc_fence_after();
-            issue_s(gs);
-            ptx::mma_commit(&bars.s_full[gs & 1]);
-            ++gs;
-            if (gs == g_end) ptx::mma_commit(&bars.q_free);  // Q no longer read
+            issue_s(gs, sp);
+            if (sp + 1 < kParts) {
+              ++sp;
+            } else {
+              sp = 0;
+              ptx::mma_commit(&bars.s_full[gs & 1]);
+              ++gs;
+              if (gs == g_end) ptx::mma_commit(&bars.q_free);  // Q no longer read
+            }
             progress = true;
           }
           if (gp < gs && ptx::mbar_test_wait(&bars.p_full[gp & 1], (gp >> 1) & 1)) {
@@ -408,6 +420,8 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
               *reinterpret_cast<uint4*>(st + c * kPageChunk + row * 128 + gr * 16) = make_uint4(0, 0, 0, 0);
             }
           }
+          ptx::fence_proxy_async();
+          ptx::mbar_arrive(&bars.stage_ready[s][0]);
         } else {
           if (tid < kPage) bars.kscale[s][row] = ksc;
           // Widen in place, in three lockstep steps of three chunks (one chunk row per
@@ -437,11 +451,12 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
                 w[x] = ptx::e4m3x2_to_bf16x2(words[gr * 2 + (x >> 1)] >> (16 * (x & 1)));
               *reinterpret_cast<uint4*>(dst + ((gr ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
+            // chunks 3k..3k+2 are ready for the score MMA (the next steps write above them)
+            ptx::fence_proxy_async();
+            ptx::mbar_arrive(&bars.stage_ready[s][k]);
           }
           if (!ok) break;
         }
-        ptx::fence_proxy_async();
-        ptx::mbar_arrive(&bars.stage_ready[s]);
       }
     }
   } else {
