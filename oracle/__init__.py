@@ -21,3 +21,8 @@ from .mla_ref import (  # noqa: F401
     mla_decode,
     lse_combine,
 )
+from .cache_ref import (  # noqa: F401
+    e4m3_encode,
+    quantize_row,
+    cache_append,
+)
