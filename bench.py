@@ -307,7 +307,7 @@ def run_gpu(args):
     res["clocks"] = clocks
 
     # ---------------- decode (bf16) and the fp8 workloads
-    def decode_entry(name):
+    def decode_entry(name, with_append=False):
         dinp = config_inputs(name)
         d = decode_to_device(dinp, dev)
         ws = torch.empty(binding.decode_workspace_size(dinp.B, dinp.H, dinp.T), dtype=torch.uint8,
@@ -324,10 +324,25 @@ def run_gpu(args):
         kv = decode_kv_bytes(dinp)
         gbs = kv / (dms * 1e-3) / 1e9
         binding.check_device_error()
-        return {"workload": name, "ms": dms, "kv_bytes": kv, "kv_gbs": world * gbs,
-                "frac_hbm": gbs / pk["hbm_gbs"],
-                "l2": "cache (%.0f MB) larger than L2; calls back to back, no flush" % (kv / 1e6),
-                "launches_per_call": 2}
+        res_d = {"workload": name, "ms": dms, "kv_bytes": kv, "kv_gbs": world * gbs,
+                 "frac_hbm": gbs / pk["hbm_gbs"],
+                 "l2": "cache (%.0f MB) larger than L2; calls back to back, no flush" % (kv / 1e6),
+                 "launches_per_call": 2}
+        if with_append:
+            # the step before decode: the q_len new rows of every sequence into the same cache
+            c_new = torch.randn((dinp.B, dinp.T, dinp.d_latent + dinp.d_rope), device=dev).to(torch.bfloat16)
+            cache, pt, lens = d["args"][2], d["args"][3], d["args"][4]
+
+            def append():
+                binding.mla_cache_append(c_new, cache, pt, lens, kv_scale=d["kwargs"]["kv_scale"])
+
+            ams = max_over_ranks(time_batch(append, args.steps, args.warmup))
+            binding.check_device_error()
+            rows = dinp.B * dinp.T
+            moved = rows * ((dinp.d_latent + dinp.d_rope) * (2 + (1 if dinp.fp8 else 2)) + (4 if dinp.fp8 else 0))
+            res_d["cache_append"] = {"us": ams * 1e3, "rows": rows, "bytes": moved,
+                                     "gbs": moved / (ams * 1e-3) / 1e9, "launches_per_call": 1}
+        return res_d
 
     def prefill_entry(name):
         pinp = config_inputs(name)
@@ -347,8 +362,8 @@ def run_gpu(args):
     launches += args.steps * 2
     if not args.quick:
         res["prefill_fp8"] = prefill_entry(PREFILL_FP8)
-        res["decode_fp8"] = decode_entry(DECODE_FP8)
-        launches += args.steps * 3
+        res["decode_fp8"] = decode_entry(DECODE_FP8, with_append=True)
+        launches += args.steps * 4
     res["gpu_launches"] = launches
     if rank == 0:
         res["cpu_baseline"] = cpu_baseline(inp_name=HEADLINE, budget_s=args.cpu_seconds)

@@ -148,6 +148,29 @@ mla_status mla_decode_noalloc(const void* q_latent, const void* q_rope, const vo
 size_t mla_decode_noalloc_max_workspace(void);
 
 /*
+ * mla_cache_append -- write the q_len new tokens of every sequence into the paged latent
+ * cache, where mla_decode reads them (the step before decode).  The pages say nothing about
+ * how the cache is filled; this follows mla_decode's cache layout and cache_lens reading.
+ *
+ *   c_new      [B, q_len, d_latent + d_rope] bf16 -- the new tokens' latent then rope row
+ *   kv_cache   [num_pages, page_size, d_latent + d_rope]  (kv_dtype: bf16 or e4m3), written
+ *   kv_scale   [num_pages, page_size] fp32, written -- required iff kv_dtype is
+ *              MLA_FP8_E4M3, must be NULL for bf16
+ *   page_table [B, max_pages_per_seq] int32, cache_lens [B] int32 -- as for mla_decode:
+ *              L_b counts the new tokens, token t goes to position L_b - q_len + t
+ * bf16 cache: the row is copied.  e4m3 cache: per token, scale = max|x| / 448 (1 when the row
+ * is all zero) in fp32, codes = e4m3(clamp(x / scale, -448, 448)) rounded to nearest even;
+ * the scale is stored next to the row.  Positions below 0 (L_b < q_len) are not written;
+ * a page index outside [0, num_pages) (or a position past max_pages_per_seq pages) skips the
+ * row and is reported through MLA_ERR_DEVICE_CHECK.  Only the target rows are touched.
+ * Supported: d_latent = 512, d_rope = 64, page_size = 64.
+ */
+mla_status mla_cache_append(const void* c_new, void* kv_cache, float* kv_scale,
+                            const int* page_table, const int* cache_lens, int B, int q_len,
+                            int d_latent, int d_rope, int page_size, int max_pages_per_seq,
+                            int num_pages, mla_dtype kv_dtype, void* stream);
+
+/*
  * mla_check_device_error -- synchronise `stream`, then read and clear the device
  * error word latched by earlier kernels of this library on the current device.
  * Returns MLA_OK, MLA_ERR_TIMEOUT or MLA_ERR_DEVICE_CHECK (or MLA_ERR_CUDA if the

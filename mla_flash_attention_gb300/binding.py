@@ -41,6 +41,8 @@ _lib.mla_decode_noalloc.argtypes = [_vp, _vp, _vp, _fp, _ip, _ip, _vp, _fp, _i, 
                                     _i, _i, _f, _i, _i, _vp]
 _lib.mla_decode_noalloc_max_workspace.restype = _sz
 _lib.mla_decode_noalloc_max_workspace.argtypes = []
+_lib.mla_cache_append.restype = _i
+_lib.mla_cache_append.argtypes = [_vp, _vp, _fp, _ip, _ip, _i, _i, _i, _i, _i, _i, _i, _i, _vp]
 _lib.mla_check_device_error.restype = _i
 _lib.mla_check_device_error.argtypes = [_vp]
 _lib.mla_last_error.restype = ctypes.c_char_p
@@ -49,7 +51,7 @@ _lib.mla_version.restype = _i
 _lib.mla_version.argtypes = []
 
 EXPORTED = ("mla_prefill", "mla_decode_workspace_size", "mla_decode", "mla_decode_noalloc",
-            "mla_decode_noalloc_max_workspace", "mla_check_device_error",
+            "mla_decode_noalloc_max_workspace", "mla_cache_append", "mla_check_device_error",
             "mla_last_error", "mla_version")
 
 
@@ -186,6 +188,30 @@ def mla_decode(q_latent, q_rope, kv_cache, page_table, cache_lens, kv_scale=None
                          workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st)
     return out, lse
+
+
+def mla_cache_append(c_new, kv_cache, page_table, cache_lens, kv_scale=None, *, stream=None):
+    """Write the q_len new tokens' rows c_new [B, q_len, dl+dr] (bf16) into the paged cache
+    (bf16, or float8_e4m3fn with per-row fp32 kv_scale [num_pages, page_size]) at positions
+    cache_lens[b] - q_len + t.  Modifies kv_cache (and kv_scale) in place."""
+    B, T, D = c_new.shape
+    num_pages, page_size, Dc = kv_cache.shape
+    fp8 = kv_cache.dtype == torch.float8_e4m3fn
+    _need(c_new, "c_new", torch.bfloat16, (B, T, D))
+    _need(kv_cache, "kv_cache", torch.float8_e4m3fn if fp8 else torch.bfloat16, (num_pages, page_size, D))
+    if fp8:
+        _need(kv_scale, "kv_scale", torch.float32, (num_pages, page_size))
+    elif kv_scale is not None:
+        raise ValueError("kv_scale is only used with an fp8 cache")
+    max_pages = page_table.shape[1]
+    _need(page_table, "page_table", torch.int32, (B, max_pages))
+    _need(cache_lens, "cache_lens", torch.int32, (B,))
+    st = _lib.mla_cache_append(_ptr(c_new), _ptr(kv_cache), _ptr(kv_scale), _ptr(page_table),
+                               _ptr(cache_lens), B, T, D - 64, 64, page_size,
+                               max_pages, num_pages, MLA_FP8_E4M3 if fp8 else MLA_BF16,
+                               _stream(stream))
+    _check(st)
+    return kv_cache, kv_scale
 
 
 def decode_noalloc_max_workspace() -> int:

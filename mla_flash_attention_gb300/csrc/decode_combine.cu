@@ -58,6 +58,9 @@ __global__ void __launch_bounds__(kCombWarps * 32) decode_combine_kernel(
     }
   }
   __syncthreads();
+  // launched as a programmatic dependent of the split kernel: everything above only read
+  // the lengths; the partials are read after the split grid has completed and flushed
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int n = s_n;
   const int c_first = n > 0 ? s_pb / s_chunk : 0, c_last = n > 0 ? (s_pb + n - 1) / s_chunk : -1;
   const int nsplit = c_last - c_first + 1;
@@ -134,11 +137,20 @@ cudaError_t launch_decode_combine(const float* part_o, const float* part_lse,
                                   const int* cache_lens, void* out, float* lse, int B, int H,
                                   int T, int max_pages, int G, cudaStream_t stream) {
   const int TH = T * H;
-  dim3 grid(B, (TH + kCombRows - 1) / kCombRows, kCombParts);
-  decode_combine_kernel<<<grid, kCombWarps * 32, 0, stream>>>(part_o, part_lse, cache_lens,
-                                                  static_cast<uint16_t*>(out), lse, B, H, T,
-                                                  max_pages, G);
-  return cudaGetLastError();
+  // programmatic dependent launch: the CTAs may start (and scan the lengths) while the split
+  // kernel drains; they wait for its completion before reading the partials
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(B, (TH + kCombRows - 1) / kCombRows, kCombParts);
+  cfg.blockDim = dim3(kCombWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_combine_kernel, part_o, part_lse, cache_lens,
+                            static_cast<uint16_t*>(out), lse, B, H, T, max_pages, G);
 }
 
 }  // namespace mla

@@ -210,19 +210,19 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
     bars.abort_flag = 0;
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&bars.stage_full[s], 1);
-      for (int k = 0; k < 3; ++k) ptx::mbar_init(&bars.stage_ready[s][k], kPrepThreads);
+      for (int k = 0; k < 3; ++k) ptx::mbar_init(&bars.stage_ready[s][k], kPrepThreads / 32);
       ptx::mbar_init(&bars.stage_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&bars.s_full[i], 1);
-      ptx::mbar_init(&bars.p_full[i], kRows);
+      ptx::mbar_init(&bars.p_full[i], kRows / 32);  // one arrival per softmax warp
     }
     ptx::mbar_init(&bars.o_done, 1);
     ptx::mbar_init(&bars.q_free, 1);
     ptx::mbar_init(&bars.q_lo_full, 1);
     ptx::mbar_init(&bars.q_cp_done, 1);
     ptx::mbar_init(&bars.q_hi_full, 1);
-    ptx::mbar_init(&bars.conv_sync, kPrepThreads);
+    ptx::mbar_init(&bars.conv_sync, kPrepThreads / 32);  // one arrival per preparation warp
     ptx::fence_barrier_init();
   }
   // Q rows T*H..127 are never loaded: keep them zero (finite scores in the padded rows)
@@ -236,6 +236,8 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
   volatile int* abort_flag = &bars.abort_flag;
+  // the LSE combine (next launch) may be scheduled now; it waits for this grid's completion
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   Segments segs;
   segs.init(p, bars.plan);
   int seq, L, lo, hi;
@@ -352,6 +354,15 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
         long long t0 = clock64();
         while (gp < g_end) {
           bool progress = false;
+          // PV first: it releases the page stage for the next load
+          if (gp < gs && ptx::mbar_test_wait(&bars.p_full[gp & 1], (gp >> 1) & 1)) {
+            ptx::tc_fence_after();
+            issue_pv(gp, gp == g_first);
+            ptx::mma_commit(&bars.o_done);
+            ptx::mma_commit(&bars.stage_empty[gp % kStages]);
+            ++gp;
+            progress = true;
+          }
           // S(gs) may run at most one page ahead of the oldest unissued PV (two S buffers)
           if (gs < g_end && gs <= gp + 1 &&
               ptx::mbar_test_wait(&bars.stage_ready[gs % kStages][sp], (gs / kStages) & 1)) {
@@ -365,14 +376,6 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
               ++gs;
               if (gs == g_end) ptx::mma_commit(&bars.q_free);  // Q no longer read
             }
-            progress = true;
-          }
-          if (gp < gs && ptx::mbar_test_wait(&bars.p_full[gp & 1], (gp >> 1) & 1)) {
-            ptx::tc_fence_after();
-            issue_pv(gp, gp == g_first);
-            ptx::mma_commit(&bars.o_done);
-            ptx::mma_commit(&bars.stage_empty[gp % kStages]);
-            ++gp;
             progress = true;
           }
           if (progress) {
@@ -394,8 +397,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
   } else if (warp < 4 || warp >= 8) {
     // -------------------------------------------------------------- stage preparation
     const int tid = warp < 4 ? threadIdx.x - 64 : threadIdx.x - 192;  // 0 .. kPrepThreads-1
-    const int row = tid & (kPage - 1);  // fp8: page row; thread group tid / 64 widens
-                                        // chunks 3 (tid / 64) .. 3 (tid / 64) + 2 of it
+    const int row = tid & (kPage - 1);  // the page row whose scale (fp8) this thread stages
     int g = 0;
     bool ok = true;
     while (ok && segs.next(seq, L, lo, hi)) {
@@ -407,6 +409,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
         const bool bad = page < 0 || page >= p.num_pages;
         if (bad && tid == 0) latch_error(p.err, kErrBadPage);
         const bool live = !bad && row < valid;
+        auto live_row = [&](int rr) { return !bad && rr < valid; };
         float ksc = 0.f;
         if constexpr (kFp8) ksc = live && tid < kPage ? __ldg(p.kv_scale + (size_t)page * kPage + row) : 0.f;
         ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.stage_full[s], (g / kStages) & 1, abort_flag, p.err));
@@ -421,39 +424,51 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
             }
           }
           ptx::fence_proxy_async();
-          ptx::mbar_arrive(&bars.stage_ready[s][0]);
+          __syncwarp();
+          if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(&bars.stage_ready[s][0]);
         } else {
           if (tid < kPage) bars.kscale[s][row] = ksc;
-          // Widen in place, in three lockstep steps of three chunks (one chunk row per
-          // thread per step).  bf16 chunk c (bytes [8c, 8c+8) KB) overlaps raw chunks 2c-9
+          // Widen in place, in three lockstep steps of three chunks (four 16-byte granules
+          // per thread per step).  bf16 chunk c (bytes [8c, 8c+8) KB) overlaps raw chunks 2c-9
           // and 2c-8 (raw chunk c' sits at [36 + 4c', 40 + 4c') KB), which are at most the
           // step's own chunks 3k..3k+2 or earlier ones: after every thread has read its raw
-          // row of the step (bounded mbarrier), the step's writes only destroy bytes that
+          // granules of the step (bounded mbarrier), the step's writes only destroy bytes that
           // were already read, and never those of a later step.
-          const int cgrp = tid >> 6;
 #pragma unroll 1
           for (int k = 0; k < 3 && ok; ++k) {
-            const int c = 3 * k + cgrp;
-            const uint4* src = reinterpret_cast<const uint4*>(st + kRawOffset + c * kRawChunk + row * 64);
+            // the step's 3 chunks are 768 granules of 16 raw bytes (64 rows x 4 per chunk);
+            // thread tid takes granules tid + 192 q, so a warp reads 512 contiguous bytes
             uint4 raw[4];
 #pragma unroll
-            for (int x = 0; x < 4; ++x) raw[x] = live ? src[x] : make_uint4(0, 0, 0, 0);
-            ptx::mbar_arrive(&bars.conv_sync);
+            for (int q = 0; q < 4; ++q) {
+              const int G = tid + kPrepThreads * q, c = 3 * k + (G >> 8), gi = G & 255;
+              raw[q] = (live_row(gi >> 2))
+                           ? *reinterpret_cast<const uint4*>(st + kRawOffset + c * kRawChunk + gi * 16)
+                           : make_uint4(0, 0, 0, 0);
+            }
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(&bars.conv_sync);
             ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.conv_sync, (3 * g + k) & 1, abort_flag, p.err));
             if (!ok) break;
-            const uint32_t* words = reinterpret_cast<const uint32_t*>(raw);
-            unsigned char* dst = st + c * kPageChunk + row * 128;
 #pragma unroll
-            for (int gr = 0; gr < 8; ++gr) {
-              uint32_t w[4];
+            for (int q = 0; q < 4; ++q) {
+              const int G = tid + kPrepThreads * q, c = 3 * k + (G >> 8), gi = G & 255;
+              const int rw = gi >> 2, quarter = gi & 3;  // 16 columns 16 quarter .. of row rw
+              const uint32_t words[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
+              uint32_t w[8];
 #pragma unroll
-              for (int x = 0; x < 4; ++x)
-                w[x] = ptx::e4m3x2_to_bf16x2(words[gr * 2 + (x >> 1)] >> (16 * (x & 1)));
-              *reinterpret_cast<uint4*>(dst + ((gr ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+              for (int x = 0; x < 4; ++x) {
+                w[2 * x] = ptx::e4m3x2_to_bf16x2(words[x]);
+                w[2 * x + 1] = ptx::e4m3x2_to_bf16x2(words[x] >> 16);
+              }
+              unsigned char* dst = st + c * kPageChunk + rw * 128;
+              *reinterpret_cast<uint4*>(dst + (((2 * quarter) ^ (rw & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+              *reinterpret_cast<uint4*>(dst + (((2 * quarter + 1) ^ (rw & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
             }
             // chunks 3k..3k+2 are ready for the score MMA (the next steps write above them)
             ptx::fence_proxy_async();
-            ptx::mbar_arrive(&bars.stage_ready[s][k]);
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(&bars.stage_ready[s][k]);
           }
           if (!ok) break;
         }
@@ -553,7 +568,8 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
         ptx::tmem_st32(s_addr, pk);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(&bars.p_full[g & 1]);
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(&bars.p_full[g & 1]);
       }
       if (!ok) break;
       // epilogue of the segment: partial (O_half / l, LSE) into slot unit + seq

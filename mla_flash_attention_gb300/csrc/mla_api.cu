@@ -30,6 +30,10 @@ cudaError_t launch_decode_sm103(const void* q_latent, const void* q_rope, const 
 cudaError_t launch_decode_combine(const float* part_o, const float* part_lse,
                                   const int* cache_lens, void* out, float* lse, int B, int H,
                                   int T, int max_pages, int G, cudaStream_t stream);
+cudaError_t launch_cache_append(const void* c_new, void* cache, float* kv_scale,
+                                const int* page_table, const int* cache_lens, int B, int T,
+                                int max_pages, int num_pages, bool fp8, unsigned int* err,
+                                cudaStream_t stream);
 }  // namespace mla
 
 namespace {
@@ -234,6 +238,41 @@ mla_status mla_decode(const void* q_latent, const void* q_rope, const void* kv_c
     e = mla::launch_decode_combine(ws.part_o, ws.part_lse, cache_lens, out, lse, B, H, q_len,
                                    max_pages_per_seq, G, st);
   if (e != cudaSuccess) return cuda_fail(e, "mla_decode launch");
+  return MLA_OK;
+}
+
+mla_status mla_cache_append(const void* c_new, void* kv_cache, float* kv_scale,
+                            const int* page_table, const int* cache_lens, int B, int q_len,
+                            int d_latent, int d_rope, int page_size, int max_pages_per_seq,
+                            int num_pages, mla_dtype kv_dtype, void* stream) {
+  if (!c_new || !kv_cache || !page_table || !cache_lens)
+    return fail(MLA_ERR_INVALID_ARG, "mla_cache_append: null tensor pointer");
+  if (B <= 0 || q_len <= 0 || max_pages_per_seq <= 0 || num_pages <= 0)
+    return fail(MLA_ERR_INVALID_ARG, "mla_cache_append: B, q_len, max_pages_per_seq, num_pages must be positive");
+  if (d_latent != 512 || d_rope != 64)
+    return fail(MLA_ERR_UNSUPPORTED, "mla_cache_append: only d_latent=512, d_rope=64 are built (got %d, %d)", d_latent, d_rope);
+  if (page_size != 64)
+    return fail(MLA_ERR_UNSUPPORTED, "mla_cache_append: only page_size=64 is built (got %d)", page_size);
+  if ((long long)B * q_len > 0x7fffffffLL / 4)
+    return fail(MLA_ERR_UNSUPPORTED, "mla_cache_append: B*q_len too large");
+  if ((long long)max_pages_per_seq * page_size > 0x7fffffffLL)
+    return fail(MLA_ERR_UNSUPPORTED, "mla_cache_append: max_pages_per_seq*page_size overflows int32");
+  const bool fp8 = kv_dtype == MLA_FP8_E4M3;
+  if (kv_dtype != MLA_BF16 && !fp8)
+    return fail(MLA_ERR_UNSUPPORTED, "mla_cache_append: kv_dtype must be MLA_BF16 or MLA_FP8_E4M3");
+  if (fp8 != (kv_scale != nullptr))
+    return fail(MLA_ERR_INVALID_ARG, "mla_cache_append: kv_scale is required for fp8 and must be NULL for bf16");
+  const void* ptrs[] = {c_new, kv_cache};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return fail(MLA_ERR_INVALID_ARG, "mla_cache_append: tensors must be 16-byte aligned");
+  if (kv_scale && (reinterpret_cast<uintptr_t>(kv_scale) & 3))
+    return fail(MLA_ERR_INVALID_ARG, "mla_cache_append: kv_scale must be 4-byte aligned");
+  unsigned int* err = device_error_word();
+  if (!err) return fail(MLA_ERR_CUDA, "mla_cache_append: device error word not reachable");
+  cudaError_t e = mla::launch_cache_append(c_new, kv_cache, kv_scale, page_table, cache_lens, B,
+                                           q_len, max_pages_per_seq, num_pages, fp8, err,
+                                           static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mla_cache_append launch");
   return MLA_OK;
 }
 

@@ -93,8 +93,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < NQ; ++t) {
       ptx::mbar_init(&bars.s_full[t], 1);
-      ptx::mbar_init(&bars.p_full[t][0], BM);
-      ptx::mbar_init(&bars.p_full[t][1], BM);
+      ptx::mbar_init(&bars.p_full[t][0], BM / 32);  // one arrival per softmax warp
+      ptx::mbar_init(&bars.p_full[t][1], BM / 32);
       ptx::mbar_init(&bars.o_done[t], 1);
     }
     ptx::fence_barrier_init();
@@ -323,7 +323,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_st32(s_addr + c * 32, pk);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(&bars.p_full[t][c]);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&bars.p_full[t][c]);
       }
       const uint64_t ps_all = ptx::add2(ps2[0], ps2[1]);
       l += ptx::f2_lo(ps_all) + ptx::f2_hi(ps_all);
