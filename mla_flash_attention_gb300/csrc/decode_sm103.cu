@@ -501,18 +501,26 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
         const bool bad = page < 0 || page >= p.num_pages;
         const int key0 = pg * kPage;
         const int lim = bad ? -1 : min(last_visible, L - 1);  // visible keys: key0+x <= lim
-        float mx8[8] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY,
-                        -INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        // unscaled scores (fp8: times the key's scale), two keys per packed instruction; the
+        // softmax scale is applied in the exponent argument
+        const float* ks = bars.kscale[g % kStages];
+        uint64_t s2[32];
 #pragma unroll
-        for (int x = 0; x < 64; ++x) {
-          float v = s[x];
-          if constexpr (kFp8) v *= bars.kscale[g % kStages][x];
-          v = (key0 + x <= lim) ? v * p.scale_log2 : -INFINITY;
-          s[x] = v;
-          mx8[x & 7] = fmaxf(mx8[x & 7], v);
+        for (int x = 0; x < 32; ++x) {
+          s2[x] = ptx::f2(s[2 * x], s[2 * x + 1]);
+          if constexpr (kFp8) s2[x] = ptx::mul2(s2[x], ptx::f2(ks[2 * x], ks[2 * x + 1]));
         }
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        if (key0 + kPage - 1 > lim) {  // a partial page (or a bad one): mask invisible keys
+#pragma unroll
+          for (int x = 0; x < 32; ++x)
+            s2[x] = ptx::f2(key0 + 2 * x <= lim ? ptx::f2_lo(s2[x]) : -INFINITY,
+                            key0 + 2 * x + 1 <= lim ? ptx::f2_hi(s2[x]) : -INFINITY);
+        }
+        float mx4[4] = {ptx::f2_lo(s2[0]), ptx::f2_hi(s2[0]), ptx::f2_lo(s2[1]), ptx::f2_hi(s2[1])};
+#pragma unroll
+        for (int x = 2; x < 32; ++x) mx4[x & 3] = ptx::fmax3(mx4[x & 3], ptx::f2_lo(s2[x]), ptx::f2_hi(s2[x]));
+        // tile maximum in the exponent domain (the scale is positive; -inf stays -inf)
+        const float mx = ptx::fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]) * p.scale_log2;
         float m_use = m;
         if (pg == lo) {
           m_use = mx;
@@ -544,25 +552,28 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
         }
         m = m_use;
         const float neg_m = (m == -INFINITY) ? 0.f : -m;
-        float ps[4] = {0.f, 0.f, 0.f, 0.f}, pr[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint64_t sc2 = ptx::f2(p.scale_log2, p.scale_log2), nm2 = ptx::f2(neg_m, neg_m);
+        uint64_t ps2[2] = {ptx::f2(0.f, 0.f), ptx::f2(0.f, 0.f)};
+        float pr[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t pk[32];
 #pragma unroll
         for (int x = 0; x < 32; ++x) {
-          const float p0 = ptx::ex2(s[2 * x] + neg_m);
-          const float p1 = ptx::ex2(s[2 * x + 1] + neg_m);
-          ps[x & 3] += p0 + p1;
+          const uint64_t a2 = ptx::fma2(s2[x], sc2, nm2);
+          const uint64_t pp = ptx::f2(ptx::ex2(ptx::f2_lo(a2)), ptx::ex2(ptx::f2_hi(a2)));
+          ps2[x & 1] = ptx::add2(ps2[x & 1], pp);
           if constexpr (kFp8) {
-            pk[x] = ptx::pack_bf16x2(p0 * bars.kscale[g % kStages][2 * x],
-                                     p1 * bars.kscale[g % kStages][2 * x + 1]);
+            const uint64_t ab = ptx::mul2(pp, ptx::f2(ks[2 * x], ks[2 * x + 1]));  // P' = p ks
+            pk[x] = ptx::pack_bf16x2(ptx::f2_lo(ab), ptx::f2_hi(ab));
           } else {
             // O is normalised by the sum of the bf16-rounded values the PV product uses
             // (exact for a dominant key); the LSE uses the exact sum
-            const uint32_t w = ptx::pack_bf16x2(p0, p1);
+            const uint32_t w = ptx::pack_bf16x2(ptx::f2_lo(pp), ptx::f2_hi(pp));
             pk[x] = w;
-            pr[x & 3] += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+            ptx::add_bf16x2(pr[2 * (x & 1)], pr[2 * (x & 1) + 1], w);
           }
         }
-        const float psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        const uint64_t ps_all = ptx::add2(ps2[0], ps2[1]);
+        const float psum = ptx::f2_lo(ps_all) + ptx::f2_hi(ps_all);
         l += psum;
         lr += kFp8 ? psum : (pr[0] + pr[1]) + (pr[2] + pr[3]);
         ptx::tmem_st32(s_addr, pk);

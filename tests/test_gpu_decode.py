@@ -100,3 +100,19 @@ def test_full_size_configs(lib, name, tol):
     o, l = run(lib, inp)
     O, L = oracle.mla_decode(inp)
     check(o, O, l, L, tol, what=name)
+
+
+def test_fp8_widening_is_exact_for_every_code(lib):
+    # One visible key whose latent columns hold every finite e4m3 code (subnormals and both
+    # zeros included) with scale 1: P' = 1 and O is that row, so the bf16 output must equal
+    # the decoded codes exactly (each e4m3 value is a bf16 value).
+    inp = make_decode(1, 1, 1, [1], fp8=True, seed=61)
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    row = np.resize(finite, 576).astype(np.uint8)
+    row[512:] = 0  # rope columns: no contribution needed
+    page = int(inp.page_table[0, 0])
+    inp.kv_cache[page, 0] = row
+    inp.kv_scale[page, 0] = 1.0
+    o, l = run(lib, inp)
+    want = oracle.e4m3_to_f64(row[:512])
+    assert np.array_equal(o[0, 0, 0], want), np.argwhere(o[0, 0, 0] != want)[:5]
