@@ -26,3 +26,4 @@ from .cache_ref import (  # noqa: F401
     quantize_row,
     cache_append,
 )
+from .absorb_ref import absorb  # noqa: F401
