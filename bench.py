@@ -172,8 +172,8 @@ class Ranks:
 
 # --------------------------------------------------------------------------- GPU arm
 
-def time_calls(fn, steps, warmup):
-    """Per-call CUDA-event times (ms) on the current stream."""
+def time_calls(fn, steps, warmup, before=None):
+    """Per-call CUDA-event times (ms) on the current stream (`before` runs outside the events)."""
     import torch
 
     for _ in range(warmup):
@@ -181,6 +181,8 @@ def time_calls(fn, steps, warmup):
     torch.cuda.synchronize()
     evs = []
     for _ in range(steps):
+        if before is not None:
+            before()
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.record()
         fn()
@@ -359,6 +361,26 @@ def run_gpu(args):
                 "frac_bf16_peak": tf / pk["bf16_tflops"], "out_dtype": "fp32"}
 
     res["decode"] = decode_entry(DECODE)
+    launches += args.steps * 2
+
+    # the absorption products either side of the bf16 decode workload (B64 T1 H128)
+    evict = torch.ones(64 << 20, dtype=torch.float32, device=dev)  # 256 MB, read to evict L2
+
+    def absorb_entry(R, H, K, N):
+        x = torch.randn((R, H, K), device=dev).to(torch.bfloat16)
+        w = (torch.randn((H, K, N), device=dev) / K ** 0.5).to(torch.bfloat16)
+        y = torch.empty((R, H, N), dtype=torch.bfloat16, device=dev)
+        ams = max_over_ranks(statistics.mean(time_calls(lambda: binding.mla_absorb(x, w, out=y),
+                                                        args.steps, args.warmup, before=evict.sum)))
+        moved = 2 * (R * H * K + H * K * N + R * H * N)
+        return {"shape": "x [%d,%d,%d] w [%d,%d,%d]" % (R, H, K, H, K, N), "us": ams * 1e3,
+                "bytes": moved, "gbs": moved / (ams * 1e-3) / 1e9,
+                "frac_hbm": moved / (ams * 1e-3) / 1e9 / pk["hbm_gbs"],
+                "l2": "256 MB read before each call (weights not L2-resident)"}
+
+    res["absorb"] = {"q_nope_W_UK": absorb_entry(64, 128, 128, 512),
+                     "O_latent_W_UV": absorb_entry(64, 128, 512, 128)}
+    binding.check_device_error()
     launches += args.steps * 2
     if not args.quick:
         res["prefill_fp8"] = prefill_entry(PREFILL_FP8)

@@ -171,6 +171,19 @@ mla_status mla_cache_append(const void* c_new, void* kv_cache, float* kv_scale,
                             int num_pages, mla_dtype kv_dtype, void* stream);
 
 /*
+ * mla_absorb -- the per-head absorption product either side of absorbed decode:
+ *     y[r, h, :] = x[r, h, :] @ w[h]      (fp32 accumulation, bf16 round-to-nearest-even out)
+ *   x [R, H, K] bf16, w [H, K, N] bf16, y [R, H, N] bf16 (all contiguous, 16-byte aligned).
+ * Before decode: x = q_nope [B*q_len, H, d_nope], w = W_UK [H, d_nope, d_latent] gives
+ * q_latent; after it: x = O_latent [B*q_len, H, d_latent], w = W_UV [H, d_latent, d_v] gives
+ * the output.  The pages only name the absorbed (latent) form of decode; this entry point is
+ * the plain product that feeds and follows it.
+ * Supported: K a multiple of 64, N a multiple of 128, R >= 1, H <= 65535.
+ */
+mla_status mla_absorb(const void* x, const void* w, void* y, int R, int H, int K, int N,
+                      void* stream);
+
+/*
  * mla_check_device_error -- synchronise `stream`, then read and clear the device
  * error word latched by earlier kernels of this library on the current device.
  * Returns MLA_OK, MLA_ERR_TIMEOUT or MLA_ERR_DEVICE_CHECK (or MLA_ERR_CUDA if the

@@ -41,6 +41,8 @@ _lib.mla_decode_noalloc.argtypes = [_vp, _vp, _vp, _fp, _ip, _ip, _vp, _fp, _i, 
                                     _i, _i, _f, _i, _i, _vp]
 _lib.mla_decode_noalloc_max_workspace.restype = _sz
 _lib.mla_decode_noalloc_max_workspace.argtypes = []
+_lib.mla_absorb.restype = _i
+_lib.mla_absorb.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _vp]
 _lib.mla_cache_append.restype = _i
 _lib.mla_cache_append.argtypes = [_vp, _vp, _fp, _ip, _ip, _i, _i, _i, _i, _i, _i, _i, _i, _vp]
 _lib.mla_check_device_error.restype = _i
@@ -51,7 +53,8 @@ _lib.mla_version.restype = _i
 _lib.mla_version.argtypes = []
 
 EXPORTED = ("mla_prefill", "mla_decode_workspace_size", "mla_decode", "mla_decode_noalloc",
-            "mla_decode_noalloc_max_workspace", "mla_cache_append", "mla_check_device_error",
+            "mla_decode_noalloc_max_workspace", "mla_cache_append", "mla_absorb",
+            "mla_check_device_error",
             "mla_last_error", "mla_version")
 
 
@@ -188,6 +191,19 @@ def mla_decode(q_latent, q_rope, kv_cache, page_table, cache_lens, kv_scale=None
                          workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st)
     return out, lse
+
+
+def mla_absorb(x, w, *, out=None, stream=None):
+    """y[r, h, :] = x[r, h, :] @ w[h] for x [R, H, K] and w [H, K, N] (bf16); returns y [R, H, N]."""
+    R, H, K = x.shape
+    N = w.shape[-1]
+    _need(x, "x", torch.bfloat16, (R, H, K))
+    _need(w, "w", torch.bfloat16, (H, K, N))
+    if out is None:
+        out = torch.empty((R, H, N), dtype=torch.bfloat16, device=x.device)
+    _need(out, "out", torch.bfloat16, (R, H, N))
+    _check(_lib.mla_absorb(_ptr(x), _ptr(w), _ptr(out), R, H, K, N, _stream(stream)))
+    return out
 
 
 def mla_cache_append(c_new, kv_cache, page_table, cache_lens, kv_scale=None, *, stream=None):

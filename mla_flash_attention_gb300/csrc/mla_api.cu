@@ -30,6 +30,8 @@ cudaError_t launch_decode_sm103(const void* q_latent, const void* q_rope, const 
 cudaError_t launch_decode_combine(const float* part_o, const float* part_lse,
                                   const int* cache_lens, void* out, float* lse, int B, int H,
                                   int T, int max_pages, int G, cudaStream_t stream);
+cudaError_t launch_absorb_sm103(const void* x, const void* w, void* y, int R, int H, int K, int N,
+                                unsigned int* err, cudaStream_t stream);
 cudaError_t launch_cache_append(const void* c_new, void* cache, float* kv_scale,
                                 const int* page_table, const int* cache_lens, int B, int T,
                                 int max_pages, int num_pages, bool fp8, unsigned int* err,
@@ -238,6 +240,25 @@ mla_status mla_decode(const void* q_latent, const void* q_rope, const void* kv_c
     e = mla::launch_decode_combine(ws.part_o, ws.part_lse, cache_lens, out, lse, B, H, q_len,
                                    max_pages_per_seq, G, st);
   if (e != cudaSuccess) return cuda_fail(e, "mla_decode launch");
+  return MLA_OK;
+}
+
+mla_status mla_absorb(const void* x, const void* w, void* y, int R, int H, int K, int N,
+                      void* stream) {
+  if (!x || !w || !y) return fail(MLA_ERR_INVALID_ARG, "mla_absorb: null tensor pointer");
+  if (R <= 0 || H <= 0 || K <= 0 || N <= 0)
+    return fail(MLA_ERR_INVALID_ARG, "mla_absorb: R, H, K, N must be positive");
+  if (K % 64 != 0 || N % 128 != 0)
+    return fail(MLA_ERR_UNSUPPORTED, "mla_absorb: K must be a multiple of 64 and N of 128 (got %d, %d)", K, N);
+  if (H > 65535 || (long long)R * H * (K > N ? K : N) > 0x7fffffffffLL)
+    return fail(MLA_ERR_UNSUPPORTED, "mla_absorb: tensor too large");
+  const void* ptrs[] = {x, w, y};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return fail(MLA_ERR_INVALID_ARG, "mla_absorb: tensors must be 16-byte aligned");
+  unsigned int* err = device_error_word();
+  if (!err) return fail(MLA_ERR_CUDA, "mla_absorb: device error word not reachable");
+  cudaError_t e = mla::launch_absorb_sm103(x, w, y, R, H, K, N, err, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mla_absorb launch");
   return MLA_OK;
 }
 
