@@ -363,6 +363,31 @@ def run_gpu(args):
     res["decode"] = decode_entry(DECODE)
     launches += args.steps * 2
 
+    def chunked_entry():
+        # chunked prefill in absorbed form: 4 sequences of 4096 tokens whose last 64 are the
+        # new chunk (rows 64 x 128 heads = 64 query tiles per sequence), bf16 cache
+        from gen import make_decode
+
+        cinp = make_decode(4, 128, 64, 4096, seed=1005)
+        cd = decode_to_device(cinp, dev)
+        out = torch.empty((cinp.B, cinp.T, cinp.H, cinp.d_latent), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((cinp.B, cinp.H, cinp.T), dtype=torch.float32, device=dev)
+        ws = torch.empty(binding.decode_workspace_size(cinp.B, cinp.H, cinp.T), dtype=torch.uint8,
+                         device=dev)
+
+        def call():
+            binding.mla_decode(*cd["args"], **cd["kwargs"], softmax_scale=cinp.softmax_scale,
+                               causal=True, out=out, lse=lse, workspace=ws)
+
+        cms = max_over_ranks(time_batch(call, args.steps, args.warmup))
+        binding.check_device_error()
+        L = cinp.cache_lens.astype(np.int64)
+        pairs = sum(int(sum(l - cinp.T + t + 1 for t in range(cinp.T))) for l in L) * cinp.H
+        f = 2.0 * pairs * (cinp.d_latent + cinp.d_rope + cinp.d_latent)
+        return {"workload": "chunk of 64 new tokens on 4032 cached, B4 H128, bf16 cache",
+                "ms": cms, "flops_absorbed": f, "tflops": world * f / (cms * 1e-3) / 1e12,
+                "launches_per_call": 2}
+
     # the absorption products either side of the bf16 decode workload (B64 T1 H128)
     evict = torch.ones(64 << 20, dtype=torch.float32, device=dev)  # 256 MB, read to evict L2
 
@@ -386,6 +411,8 @@ def run_gpu(args):
         res["prefill_fp8"] = prefill_entry(PREFILL_FP8)
         res["decode_fp8"] = decode_entry(DECODE_FP8, with_append=True)
         launches += args.steps * 4
+        res["chunked_prefill"] = chunked_entry()
+        launches += args.steps * 2
     res["gpu_launches"] = launches
     if rank == 0:
         res["cpu_baseline"] = cpu_baseline(inp_name=HEADLINE, budget_s=args.cpu_seconds)

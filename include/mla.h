@@ -110,7 +110,9 @@ size_t mla_decode_workspace_size(int B, int H, int q_len, int d_latent);
  * 0 .. L_b - 1.  Cache rows past L_b may hold anything (even NaN): they are
  * never mixed into a result.  Page indices must lie in [0, num_pages): entries
  * outside are reported through MLA_ERR_DEVICE_CHECK (that page is skipped).
- * Supported: d_latent = 512, d_rope = 64, page_size = 64, q_len * H <= 128.
+ * Supported: d_latent = 512, d_rope = 64, page_size = 64, q_len * H <= 65536 (rows beyond
+ * 128 are processed in tiles of 128 rows: q_len > 1 new tokens over a cached prefix is
+ * chunked prefill in absorbed form, after mla_cache_append has written the chunk's rows).
  */
 mla_status mla_decode(const void* q_latent, const void* q_rope, const void* kv_cache,
                       const float* kv_scale, const int* page_table, const int* cache_lens,

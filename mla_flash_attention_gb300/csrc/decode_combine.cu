@@ -31,6 +31,10 @@ __global__ void __launch_bounds__(kCombWarps * 32) decode_combine_kernel(
   const int TH = T * H;
   const int row0 = blockIdx.y * kCombRows;
   const int nrows = min(kCombRows, TH - row0);
+  // the rows are planned in query tiles of 128 (TQ = min(TH, 128) rows each): this CTA's 32
+  // rows lie in tile qt, whose work item is the virtual sequence b * NQT + qt
+  const int NQT = (TH + 127) / 128, TQ = TH < 128 ? TH : 128;
+  const int qt = row0 / 128, r0 = row0 % 128, v = b * NQT + qt;
   const int q_base = blockIdx.z * kCombQuads;
   __shared__ int s_pb, s_n, s_chunk;
   __shared__ __align__(16) uint16_t s_out[kCombRows][kCombQuads * 4];
@@ -51,9 +55,10 @@ __global__ void __launch_bounds__(kCombWarps * 32) decode_combine_kernel(
       before += nb;
       total += nt;
     }
-    if (lane == 0) {
-      s_pb = before;
+    if (lane == 0) {  // every sequence is planned NQT times (once per query tile)
       s_n = pages_of(comb_clamp_len(__ldg(cache_lens + b), max_pages), kCombPage);
+      s_pb = before * NQT + qt * s_n;
+      total *= NQT;
       s_chunk = total > 0 ? (total + G - 1) / G : 1;
     }
   }
@@ -74,25 +79,25 @@ __global__ void __launch_bounds__(kCombWarps * 32) decode_combine_kernel(
   if (live && nsplit > 0) {
     // every thread weighs the splits of its own row: w_s = exp(lse_s - max) / sum; the
     // partial loads of the first two splits are issued before the weights are known
-    const size_t slot_stride = (size_t)128 * TH;
+    const size_t slot_stride = (size_t)128 * TQ;
     const float4* src = reinterpret_cast<const float4*>(part_o) +
-                        ((size_t)(c_first + b) * 128 + q_base + warp) * TH + row;
-    const float* lsp = part_lse + ((size_t)c_first + b) * TH + row;
+                        ((size_t)(c_first + v) * 128 + q_base + warp) * TQ + r0 + lane;
+    const float* lsp = part_lse + ((size_t)c_first + v) * TQ + r0 + lane;
     float4 a[2][kQ];
 #pragma unroll
     for (int u = 0; u < 2; ++u)
 #pragma unroll
       for (int j = 0; j < kQ; ++j)
-        a[u][j] = u < nsplit ? __ldg(src + (size_t)u * slot_stride + (size_t)j * kCombWarps * TH)
+        a[u][j] = u < nsplit ? __ldg(src + (size_t)u * slot_stride + (size_t)j * kCombWarps * TQ)
                              : make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k = 0; k < nsplit; ++k) mx = fmaxf(mx, __ldg(lsp + (size_t)k * TH));
+    for (int k = 0; k < nsplit; ++k) mx = fmaxf(mx, __ldg(lsp + (size_t)k * TQ));
     for (int k = 0; k < nsplit; ++k) {
-      const float ls = __ldg(lsp + (size_t)k * TH);
+      const float ls = __ldg(lsp + (size_t)k * TQ);
       wsum += (mx == -INFINITY || ls == -INFINITY) ? 0.f : __expf(ls - mx);
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
     auto weight = [&](int k) -> float {
-      const float ls = __ldg(lsp + (size_t)k * TH);
+      const float ls = __ldg(lsp + (size_t)k * TQ);
       return (mx == -INFINITY || ls == -INFINITY) ? 0.f : __expf(ls - mx) * inv;
     };
     for (int k = 0; k < nsplit; k += 2) {
@@ -101,7 +106,7 @@ __global__ void __launch_bounds__(kCombWarps * 32) decode_combine_kernel(
         for (int u = 0; u < 2; ++u)
 #pragma unroll
           for (int j = 0; j < kQ; ++j)
-            a[u][j] = k + u < nsplit ? __ldg(src + (size_t)(k + u) * slot_stride + (size_t)j * kCombWarps * TH)
+            a[u][j] = k + u < nsplit ? __ldg(src + (size_t)(k + u) * slot_stride + (size_t)j * kCombWarps * TQ)
                                      : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll

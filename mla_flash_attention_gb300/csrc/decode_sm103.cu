@@ -60,6 +60,7 @@ struct Params {
   float* part_lse;
   unsigned int* err;
   int B, H, T, max_pages, num_pages, causal, G;
+  int NQT, TQ;  // query tiles per sequence (T*H rows in tiles of 128) and rows per tile
   float scale_log2;
 };
 
@@ -95,9 +96,9 @@ __device__ __forceinline__ int warp_sum(int v) {
 // (256 at a time) and warp scans.
 __device__ void make_plan(const Params& prm, int unit, Plan* out) {
   const int lane = threadIdx.x & 31;
-  const int B = prm.B;
+  const int B = prm.B * prm.NQT;  // work is planned per (sequence, query tile)
   auto pages_at = [&](int bb) {
-    return bb < B ? pages_of(clamp_len(__ldg(prm.cache_lens + bb), prm.max_pages), kPage) : 0;
+    return bb < B ? pages_of(clamp_len(__ldg(prm.cache_lens + bb / prm.NQT), prm.max_pages), kPage) : 0;
   };
   int total = 0;
   for (int base = 0; base < B; base += 256) {
@@ -145,24 +146,26 @@ __device__ void make_plan(const Params& prm, int unit, Plan* out) {
 // role runs its own copy and sees the same sequence.
 struct Segments {
   const int* lens;
-  int B, max_pages, start, end, b, pb;
+  int B, NQT, max_pages, start, end, b, pb;
   __device__ void init(const Params& prm, const Plan& plan) {
     lens = prm.cache_lens;
-    B = prm.B;
+    NQT = prm.NQT;
+    B = prm.B * prm.NQT;
     max_pages = prm.max_pages;
     start = plan.start;
     end = plan.end;
     b = plan.b0;
     pb = plan.pb0;
   }
-  // Next non-empty segment: sets seq, L, lo, hi (page indices within the sequence).
+  // Next non-empty segment: sets seq (the virtual sequence: sequence * NQT + query tile),
+  // L, lo, hi (page indices within the sequence).
   // Lengths are fetched eight at a time so that skipping to this unit's first sequence
   // costs one load latency per eight sequences rather than one per sequence.
   __device__ bool next(int& seq, int& L, int& lo, int& hi) {
     while (b < B && pb < end) {
       int Ls[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) Ls[i] = b + i < B ? __ldg(lens + b + i) : 0;
+      for (int i = 0; i < 8; ++i) Ls[i] = b + i < B ? __ldg(lens + (b + i) / NQT) : 0;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         if (b >= B || pb >= end) return false;
@@ -185,8 +188,8 @@ struct Segments {
   }
 };
 
-__device__ __forceinline__ int page_row(const Params& p, int seq, int pg) {
-  const int page = __ldg(p.page_table + (size_t)seq * p.max_pages + pg);
+__device__ __forceinline__ int page_row(const Params& p, int vseq, int pg) {
+  const int page = __ldg(p.page_table + (size_t)(vseq / p.NQT) * p.max_pages + pg);
   // an out-of-range page reads as zeros (coordinates outside the tensor) and is masked
   return (page >= 0 && page < p.num_pages) ? page * kPage : -2 * kPage;
 }
@@ -204,7 +207,9 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
   constexpr int kParts = kFp8 ? 3 : 1;  // readiness parts of a page stage
   const int warp = threadIdx.x >> 5;
   const int unit = blockIdx.x >> 1, half = blockIdx.x & 1;
-  const int TH = p.T * p.H;
+  const int TH = p.T * p.H, TQ = p.TQ;
+  // first Q row of virtual sequence v: its sequence's rows, then 128 per query tile
+  auto q_row0 = [&](int v) { return (v / p.NQT) * TH + (v % p.NQT) * kRows; };
 
   if (threadIdx.x == 0) {
     bars.abort_flag = 0;
@@ -254,19 +259,19 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
         if (nseg == 0) {
           // first sequence: Q latent 0..255 staged in the (still unused) second page stage,
           // the rest of Q straight into the Q area, all at once
-          ptx::mbar_arrive_expect_tx(&bars.q_lo_full, 4 * TH * 128);
+          ptx::mbar_arrive_expect_tx(&bars.q_lo_full, 4 * TQ * 128);
           for (int c = 0; c < 4; ++c)
-            ptx::tma_load_2d(sm + kOffStage + kStageBytes + c * kQChunk, &tm_qlat, &bars.q_lo_full, c * 64, seq * TH);
-          ptx::mbar_arrive_expect_tx(&bars.q_hi_full, 5 * TH * 128);
+            ptx::tma_load_2d(sm + kOffStage + kStageBytes + c * kQChunk, &tm_qlat, &bars.q_lo_full, c * 64, q_row0(seq));
+          ptx::mbar_arrive_expect_tx(&bars.q_hi_full, 5 * TQ * 128);
           for (int c = 0; c < 4; ++c)
-            ptx::tma_load_2d(sm + kOffQhi + c * kQChunk, &tm_qlat, &bars.q_hi_full, 256 + c * 64, seq * TH);
-          ptx::tma_load_2d(sm + kOffQhi + 4 * kQChunk, &tm_qrope, &bars.q_hi_full, 0, seq * TH);
+            ptx::tma_load_2d(sm + kOffQhi + c * kQChunk, &tm_qlat, &bars.q_hi_full, 256 + c * 64, q_row0(seq));
+          ptx::tma_load_2d(sm + kOffQhi + 4 * kQChunk, &tm_qrope, &bars.q_hi_full, 0, q_row0(seq));
         } else {
           // Q latent 0..255 into the Q area once the previous sequence's last S is done
           if (!(ok = ptx::mbar_wait(&bars.q_free, (nseg - 1) & 1, abort_flag, p.err))) break;
-          ptx::mbar_arrive_expect_tx(&bars.q_lo_full, 4 * TH * 128);
+          ptx::mbar_arrive_expect_tx(&bars.q_lo_full, 4 * TQ * 128);
           for (int c = 0; c < 4; ++c)
-            ptx::tma_load_2d(sm + kOffQhi + c * kQChunk, &tm_qlat, &bars.q_lo_full, c * 64, seq * TH);
+            ptx::tma_load_2d(sm + kOffQhi + c * kQChunk, &tm_qlat, &bars.q_lo_full, c * 64, q_row0(seq));
         }
         ++nseg;
         for (int pg = lo; pg < hi; ++pg, ++g) {
@@ -341,10 +346,10 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
         ptx::mma_commit(&bars.q_cp_done);
         if (nseg > 0) {  // the rest of Q over the staging copy (the producer loaded the first)
           if (!(ok = ptx::mbar_wait(&bars.q_cp_done, nseg & 1, abort_flag, p.err))) break;
-          ptx::mbar_arrive_expect_tx(&bars.q_hi_full, 5 * TH * 128);
+          ptx::mbar_arrive_expect_tx(&bars.q_hi_full, 5 * TQ * 128);
           for (int c = 0; c < 4; ++c)
-            ptx::tma_load_2d(sm + kOffQhi + c * kQChunk, &tm_qlat, &bars.q_hi_full, 256 + c * 64, seq * TH);
-          ptx::tma_load_2d(sm + kOffQhi + 4 * kQChunk, &tm_qrope, &bars.q_hi_full, 0, seq * TH);
+            ptx::tma_load_2d(sm + kOffQhi + c * kQChunk, &tm_qlat, &bars.q_hi_full, 256 + c * 64, q_row0(seq));
+          ptx::tma_load_2d(sm + kOffQhi + 4 * kQChunk, &tm_qrope, &bars.q_hi_full, 0, q_row0(seq));
         }
         if (!(ok = ptx::mbar_wait(&bars.q_hi_full, nseg & 1, abort_flag, p.err))) break;
         ptx::tc_fence_after();
@@ -405,9 +410,9 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
         const int s = g % kStages;
         unsigned char* st = sm + kOffStage + s * kStageBytes;
         const int valid = min(kPage, L - pg * kPage);  // rows holding tokens of this sequence
-        const int page = __ldg(p.page_table + (size_t)seq * p.max_pages + pg);
+        const int page = __ldg(p.page_table + (size_t)(seq / p.NQT) * p.max_pages + pg);
         const bool bad = page < 0 || page >= p.num_pages;
-        if (bad && tid == 0) latch_error(p.err, kErrBadPage);
+        if (bad && tid == 0 && seq % p.NQT == 0) latch_error(p.err, kErrBadPage);
         const bool live = !bad && row < valid;
         auto live_row = [&](int rr) { return !bad && rr < valid; };
         float ksc = 0.f;
@@ -478,10 +483,11 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
     // -------------------------------------------------------------- softmax / epilogue
     const int r = threadIdx.x - 128;  // query row == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const int t_row = r / p.H;
     int g = 0;
     bool ok = true;
     while (ok && segs.next(seq, L, lo, hi)) {
+      const int gr = (seq % p.NQT) * kRows + r;  // row within the sequence's T*H rows
+      const int t_row = gr / p.H;
       const int last_visible = p.causal ? (L - p.T + t_row) : (L - 1);  // keys <= this are visible
       float m = -INFINITY, l = 0.f, lr = 0.f;  // exact row sum (LSE) and bf16-rounded (PV)
       const uint32_t o_addr = tmem + lane_off + 256;
@@ -497,7 +503,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
           ptx::tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(su + 32));
           ptx::tmem_ld_wait();
         }
-        const int page = __ldg(p.page_table + (size_t)seq * p.max_pages + pg);
+        const int page = __ldg(p.page_table + (size_t)(seq / p.NQT) * p.max_pages + pg);
         const bool bad = page < 0 || page >= p.num_pages;
         const int key0 = pg * kPage;
         const int lim = bad ? -1 : min(last_visible, L - 1);  // visible keys: key0+x <= lim
@@ -591,25 +597,25 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
       const float inv = lr > 0.f ? 1.f / lr : 0.f;
       // partial layout [slot][column quad (128)][row (T*H)][4]: the 32 rows of a warp
       // store one quad as 512 contiguous bytes
-      float4* dst = reinterpret_cast<float4*>(p.part_o) + (slot * 128 + half * 64) * TH + r;
+      float4* dst = reinterpret_cast<float4*>(p.part_o) + (slot * 128 + half * 64) * TQ + r;
 #pragma unroll 1
       for (int c = 0; c < 8; c += 2) {
         uint32_t v[2][32];
         ptx::tmem_ld32(o_addr + c * 32, v[0]);
         ptx::tmem_ld32(o_addr + (c + 1) * 32, v[1]);
         ptx::tmem_ld_wait();
-        if (r < TH) {
+        if (r < TQ && gr < TH) {
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
             for (int x = 0; x < 8; ++x)
-              dst[(size_t)((c + h2) * 8 + x) * TH] =
+              dst[(size_t)((c + h2) * 8 + x) * TQ] =
                   make_float4(__uint_as_float(v[h2][4 * x]) * inv, __uint_as_float(v[h2][4 * x + 1]) * inv,
                               __uint_as_float(v[h2][4 * x + 2]) * inv, __uint_as_float(v[h2][4 * x + 3]) * inv);
         }
       }
-      if (half == 0 && r < TH)
-        p.part_lse[slot * TH + r] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+      if (half == 0 && r < TQ && gr < TH)
+        p.part_lse[slot * TQ + r] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
       ptx::tc_fence_before();
     }
   }
@@ -651,7 +657,8 @@ cudaError_t launch_decode_sm103(const void* q_latent, const void* q_rope, const 
   CUtensorMap tm_qlat, tm_qrope;
   uint64_t qdims[2] = {(uint64_t)kDl, (uint64_t)B * TH};
   uint64_t qstrides[1] = {(uint64_t)kDl * 2};
-  uint32_t qbox[2] = {64, (uint32_t)TH};
+  const int TQ = TH < 128 ? TH : 128;
+  uint32_t qbox[2] = {64, (uint32_t)TQ};
   e = encode_tensor_map_swz(&tm_qlat, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q_latent, qdims, qstrides, qbox, true);
   if (e != cudaSuccess) return e;
   qdims[0] = 64;
@@ -670,6 +677,8 @@ cudaError_t launch_decode_sm103(const void* q_latent, const void* q_rope, const 
   p.B = B;
   p.H = H;
   p.T = T;
+  p.NQT = (TH + 127) / 128;
+  p.TQ = TQ;
   p.max_pages = max_pages;
   p.num_pages = num_pages;
   p.causal = causal;

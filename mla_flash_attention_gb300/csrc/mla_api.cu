@@ -92,11 +92,15 @@ struct DecodeWorkspace {
   size_t bytes;
 };
 
+// The q_len*H query rows of a sequence are processed in tiles of (up to) 128 rows; each
+// (sequence, tile) is planned as its own work item, so there are G + B * NQT partial slots of
+// TQ = min(q_len*H, 128) rows each.
 DecodeWorkspace decode_workspace_layout(void* base, int B, int TH, int d_latent, int G) {
   DecodeWorkspace w;
-  const size_t slots = (size_t)G + (size_t)B;
-  const size_t o_bytes = align_up(slots * TH * d_latent * sizeof(float), 256);
-  const size_t l_bytes = align_up(slots * TH * sizeof(float), 256);
+  const size_t nqt = (size_t)(TH + 127) / 128, tq = TH < 128 ? TH : 128;
+  const size_t slots = (size_t)G + (size_t)B * nqt;
+  const size_t o_bytes = align_up(slots * tq * d_latent * sizeof(float), 256);
+  const size_t l_bytes = align_up(slots * tq * sizeof(float), 256);
   w.part_o = static_cast<float*>(base);
   w.part_lse = reinterpret_cast<float*>(static_cast<char*>(base) + o_bytes);
   w.bytes = o_bytes + l_bytes;
@@ -208,8 +212,10 @@ mla_status mla_decode(const void* q_latent, const void* q_rope, const void* kv_c
     return fail(MLA_ERR_UNSUPPORTED, "mla_decode: only d_latent=512, d_rope=64 are built (got %d, %d)", d_latent, d_rope);
   if (page_size != 64)
     return fail(MLA_ERR_UNSUPPORTED, "mla_decode: only page_size=64 is built (got %d)", page_size);
-  if (H * q_len > 128)
-    return fail(MLA_ERR_UNSUPPORTED, "mla_decode: q_len*H must be at most 128 (got %d)", H * q_len);
+  if ((long long)H * q_len > 65536)
+    return fail(MLA_ERR_UNSUPPORTED, "mla_decode: q_len*H must be at most 65536 (got %lld)", (long long)H * q_len);
+  if ((long long)B * ((H * q_len + 127) / 128) > (1LL << 24))
+    return fail(MLA_ERR_UNSUPPORTED, "mla_decode: B * ceil(q_len*H / 128) must be at most 2^24");
   if (B > 65535) return fail(MLA_ERR_UNSUPPORTED, "mla_decode: B must be at most 65535");
   if ((long long)max_pages_per_seq * page_size > 0x7fffffffLL)
     return fail(MLA_ERR_UNSUPPORTED, "mla_decode: max_pages_per_seq*page_size overflows int32");

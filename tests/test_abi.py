@@ -90,7 +90,7 @@ def test_decode_argument_checks(clib):
     assert _decode(clib, B=0) == 1
     assert _decode(clib, dl=256) == 2
     assert _decode(clib, ps=32) == 2
-    assert _decode(clib, H=128, T=2) == 2      # more than 128 query rows
+    assert _decode(clib, H=128, T=513) == 2    # more than 65536 query rows per sequence
     assert _decode(clib, dt=1) == 1            # fp8 without scales
     assert _decode(clib, ks=16) == 1           # bf16 with scales
     assert _decode(clib, out=8) == 1           # misaligned

@@ -116,3 +116,28 @@ def test_fp8_widening_is_exact_for_every_code(lib):
     o, l = run(lib, inp)
     want = oracle.e4m3_to_f64(row[:512])
     assert np.array_equal(o[0, 0, 0], want), np.argwhere(o[0, 0, 0] != want)[:5]
+
+
+# ---------------------------------------------------------------- query rows beyond one tile
+# q_len * H > 128: the rows of a sequence are processed in tiles of 128 (each planned as its
+# own work item); q_len new tokens over a paged prefix is chunked prefill in absorbed form.
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("B,H,T,lens", [
+    (2, 128, 4, [300, 1000]),          # 512 rows: 4 full tiles
+    (3, 40, 5, [5, 130, 777]),         # 200 rows: a full tile and a 72-row tail
+    (2, 16, 64, [64, 2000]),           # 1024 rows: a 64-token chunk over a prefix
+    (1, 3, 50, [49]),                  # 150 rows, L < q_len (the first token sees nothing)
+])
+def test_query_rows_beyond_one_tile(lib, fp8, B, H, T, lens):
+    inp = make_decode(B, H, T, lens, fp8=fp8, seed=B * 100 + H + T)
+    o, l = run(lib, inp)
+    O, L = oracle.mla_decode(inp)
+    check(o, O, l, L, TOL_O_FP8 if fp8 else TOL_O_BF16, what="B=%d H=%d T=%d fp8=%d" % (B, H, T, fp8))
+
+
+def test_chunked_prefill_chunk_of_32_tokens_at_128_heads(lib):
+    inp = make_decode(2, 128, 32, [1024, 3000], seed=77)
+    o, l = run(lib, inp)
+    O, L = oracle.mla_decode(inp)
+    check(o, O, l, L, TOL_O_BF16, what="chunk T=32 H=128")
