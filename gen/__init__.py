@@ -9,6 +9,7 @@ from .inputs import (  # noqa: F401
     PrefillInputs,
     DecodeInputs,
     make_prefill,
+    make_grad_out,
     make_decode,
     CONFIGS,
     config_inputs,

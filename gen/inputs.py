@@ -29,7 +29,7 @@ _CHUNK = 1 << 22  # elements per independently seeded chunk
 E4M3_MAX = 448.0
 
 # tensor ids (part of every SeedSequence key)
-_T_QN, _T_QR, _T_KN, _T_KR, _T_V, _T_MQ, _T_MK, _T_CACHE, _T_LENS, _T_PERM = range(10)
+_T_QN, _T_QR, _T_KN, _T_KR, _T_V, _T_MQ, _T_MK, _T_CACHE, _T_LENS, _T_PERM, _T_DO = range(11)
 
 
 def _threads() -> int:
@@ -200,6 +200,11 @@ def make_prefill(B, H, S, d_nope=128, d_rope=64, d_v=128, *, fp8=False, seed=0,
     return PrefillInputs(B, H, S, d_nope, d_rope, d_v, float(softmax_scale), bool(causal), True,
                          q_nope.reshape(B, S, H, d_nope), q_rope, k_nope, k_rope, v,
                          q_scale.reshape(B, S), k_scale.reshape(B, S), seed)
+
+
+def make_grad_out(B, S, H, d_v=128, *, seed=0) -> np.ndarray:
+    """Upstream gradient dO ``[B,S,H,d_v]`` of a prefill output: N(0,1) rounded to bf16 bits."""
+    return _bf16_normal(seed, _T_DO, (B, S, H, d_v))
 
 
 def make_decode(B, H, T, cache_lens, *, d_latent=512, d_rope=64, page_size=64, fp8=False,

@@ -27,3 +27,4 @@ from .cache_ref import (  # noqa: F401
     cache_append,
 )
 from .absorb_ref import absorb  # noqa: F401
+from .backward_ref import prefill_backward_bh, mla_prefill_backward  # noqa: F401
