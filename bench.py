@@ -363,6 +363,43 @@ def run_gpu(args):
     res["decode"] = decode_entry(DECODE)
     launches += args.steps * 2
 
+    def backward_entry():
+        # gradients of the headline prefill (B4 H128 S4096 causal) for a random upstream dO:
+        # the forward runs once outside the timed region, then prep + backward per call
+        binp = config_inputs(HEADLINE)
+        bt = prefill_to_device(binp, dev)["args"][:5]
+        out, lse = binding.mla_prefill(*bt, None, None, softmax_scale=binp.softmax_scale, causal=True)
+        d_out = torch.randn_like(out, dtype=torch.float32).to(torch.bfloat16)
+        B_, S_, H_ = binp.B, binp.S, binp.H
+        grads = (torch.empty((B_, S_, H_, 128), dtype=torch.bfloat16, device=dev),
+                 torch.empty((B_, S_, H_, 64), dtype=torch.bfloat16, device=dev),
+                 torch.empty((B_, S_, H_, 128), dtype=torch.bfloat16, device=dev),
+                 torch.empty((B_, S_, 64), dtype=torch.float32, device=dev),
+                 torch.empty((B_, S_, H_, 128), dtype=torch.bfloat16, device=dev))
+        ws = torch.empty(binding.prefill_backward_workspace_size(B_, H_, S_), dtype=torch.uint8,
+                         device=dev)
+
+        def call():
+            binding.mla_prefill_backward(*bt, out, lse, d_out, softmax_scale=binp.softmax_scale,
+                                         causal=True, grads=grads, workspace=ws)
+
+        barrier()
+        bms = max_over_ranks(statistics.mean(time_calls(call, args.steps, args.warmup)))
+        binding.check_device_error()
+        # algorithmic FLOP per visible (query, key) pair: S = Q K' (192), dP = dO V' (128),
+        # dV (128), dQ (192), dK (192), two FLOP per multiply-add
+        f = prefill_flops(B_, H_, S_) * (192 + 128 + 128 + 192 + 192) / (192 + 128)
+        tf = f / (bms * 1e-3) / 1e12
+        return {"workload": "backward of " + HEADLINE, "ms": bms, "flops": f,
+                "tflops": world * tf, "frac_bf16_peak": tf / pk["bf16_tflops"],
+                "flop_per_pair": 2 * (192 + 128 + 128 + 192 + 192),
+                "issued_flop_per_pair": 2 * (2 * 192 + 2 * 128 + 128 + 192 + 192),
+                "l2": "inputs (2.7 GB) larger than L2; no flush", "launches_per_call": 2}
+
+    res["prefill_backward"] = backward_entry()
+    launches += args.steps * 2
+    torch.cuda.empty_cache()
+
     def chunked_entry():
         # chunked prefill in absorbed form: 4 sequences of 4096 tokens whose last 64 are the
         # new chunk (rows 64 x 128 heads = 64 query tiles per sequence), bf16 cache
@@ -499,6 +536,7 @@ PROFILE_CASES = {
     "decode": dict(kind="decode", B=32, H=128, T=1, lens=4096, fp8=False, seed=1003),
     "decode_fp8": dict(kind="decode", B=64, H=16, T=2, lens=("uniform", 1, 8192), fp8=True,
                        seed=1004),
+    "backward": dict(kind="backward", B=1, H=64, S=4096, fp8=False, seed=1001),
 }
 
 
@@ -517,6 +555,13 @@ def run_profile_case(name):
         t = prefill_to_device(inp, dev)
         for _ in range(3):
             binding.mla_prefill(*t["args"], softmax_scale=inp.softmax_scale, causal=True)
+    elif c["kind"] == "backward":
+        inp = make_prefill(c["B"], c["H"], c["S"], seed=c["seed"])
+        t = prefill_to_device(inp, dev)["args"][:5]
+        out, lse = binding.mla_prefill(*t, None, None, softmax_scale=inp.softmax_scale, causal=True)
+        d_out = torch.randn_like(out, dtype=torch.float32).to(torch.bfloat16)
+        for _ in range(3):
+            binding.mla_prefill_backward(*t, out, lse, d_out, softmax_scale=inp.softmax_scale)
     else:
         inp = make_decode(c["B"], c["H"], c["T"], c["lens"], fp8=c["fp8"], seed=c["seed"])
         d = decode_to_device(inp, dev)

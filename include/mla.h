@@ -186,6 +186,38 @@ mla_status mla_absorb(const void* x, const void* w, void* y, int R, int H, int K
                       void* stream);
 
 /*
+ * mla_prefill_backward_workspace_size -- bytes of device workspace mla_prefill_backward
+ * needs (two fp32 vectors of B * H * ceil(S / 128) * 128 entries).
+ */
+size_t mla_prefill_backward_workspace_size(int B, int H, int S);
+
+/*
+ * mla_prefill_backward -- gradients of bf16 MLA prefill with respect to its operands.
+ * The pages define the forward step only (S = Q K', O += P V); this is its exact derivative
+ * for an upstream gradient d_out, reusing the forward's O and LSE:
+ *   P = exp(s - LSE),  dV = P' dO,  dP = dO V',  D_i = sum_d dO_id O_id,  dS = P * (dP - D),
+ *   dQ = softmax_scale dS [Kn|Kr],  dK = softmax_scale dS' [Qn|Qr]
+ * per (batch, head); the rope key is shared by the heads, so dk_rope is the sum over heads.
+ *
+ *   q_nope, q_rope, k_nope, k_rope, v   the forward's bf16 inputs (layouts of mla_prefill)
+ *   out     [B, S, H, d_v] bf16 -- the forward's output;  lse [B, H, S] fp32 -- its LSE
+ *   d_out   [B, S, H, d_v] bf16 -- upstream gradient
+ *   dq_nope [B, S, H, d_nope] bf16, dq_rope [B, S, H, d_rope] bf16,
+ *   dk_nope [B, S, H, d_nope] bf16, dv [B, S, H, d_v] bf16   -- written in full
+ *   dk_rope [B, S, d_rope] fp32 -- written in full (zeroed, then accumulated over heads)
+ *   workspace  device buffer of at least mla_prefill_backward_workspace_size() bytes
+ * causal as for mla_prefill.  All gradients are accumulated in fp32; P and dS enter the
+ * products as bf16.  Supported: d_nope = 128, d_rope = 64, d_v = 128, bf16 only.
+ */
+mla_status mla_prefill_backward(const void* q_nope, const void* q_rope, const void* k_nope,
+                                const void* k_rope, const void* v, const void* out,
+                                const float* lse, const void* d_out, void* dq_nope,
+                                void* dq_rope, void* dk_nope, float* dk_rope, void* dv, int B,
+                                int H, int S, int d_nope, int d_rope, int d_v,
+                                float softmax_scale, int causal, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/*
  * mla_check_device_error -- synchronise `stream`, then read and clear the device
  * error word latched by earlier kernels of this library on the current device.
  * Returns MLA_OK, MLA_ERR_TIMEOUT or MLA_ERR_DEVICE_CHECK (or MLA_ERR_CUDA if the

@@ -45,6 +45,11 @@ _lib.mla_absorb.restype = _i
 _lib.mla_absorb.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _vp]
 _lib.mla_cache_append.restype = _i
 _lib.mla_cache_append.argtypes = [_vp, _vp, _fp, _ip, _ip, _i, _i, _i, _i, _i, _i, _i, _i, _vp]
+_lib.mla_prefill_backward_workspace_size.restype = _sz
+_lib.mla_prefill_backward_workspace_size.argtypes = [_i, _i, _i]
+_lib.mla_prefill_backward.restype = _i
+_lib.mla_prefill_backward.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _fp, _vp, _vp, _vp, _vp, _fp,
+                                      _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp]
 _lib.mla_check_device_error.restype = _i
 _lib.mla_check_device_error.argtypes = [_vp]
 _lib.mla_last_error.restype = ctypes.c_char_p
@@ -54,6 +59,7 @@ _lib.mla_version.argtypes = []
 
 EXPORTED = ("mla_prefill", "mla_decode_workspace_size", "mla_decode", "mla_decode_noalloc",
             "mla_decode_noalloc_max_workspace", "mla_cache_append", "mla_absorb",
+            "mla_prefill_backward_workspace_size", "mla_prefill_backward",
             "mla_check_device_error",
             "mla_last_error", "mla_version")
 
@@ -147,6 +153,56 @@ def mla_prefill(q_nope, q_rope, k_nope, k_rope, v, q_scale=None, k_scale=None, *
                           MLA_FP32 if out_dtype == torch.float32 else MLA_BF16, _stream(stream))
     _check(st)
     return out, lse
+
+
+def prefill_backward_workspace_size(B: int, H: int, S: int) -> int:
+    return int(_lib.mla_prefill_backward_workspace_size(B, H, S))
+
+
+def mla_prefill_backward(q_nope, q_rope, k_nope, k_rope, v, out, lse, d_out, *,
+                         softmax_scale: float, causal: bool = True, grads=None, workspace=None,
+                         stream=None):
+    """Gradients of bf16 MLA prefill.  Returns (dq_nope, dq_rope, dk_nope, dk_rope, dv).
+
+    out/lse are the forward's results, d_out the upstream gradient [B,S,H,d_v] bf16.
+    dk_rope [B,S,d_rope] is fp32 (summed over heads); the others are bf16 in the layouts of
+    their operands.  ``grads`` may pass those five tensors preallocated.
+    """
+    B, S, H, dn = q_nope.shape
+    dr = q_rope.shape[-1]
+    dv_ = v.shape[-1]
+    bf = torch.bfloat16
+    _need(q_nope, "q_nope", bf, (B, S, H, dn))
+    _need(q_rope, "q_rope", bf, (B, S, H, dr))
+    _need(k_nope, "k_nope", bf, (B, S, H, dn))
+    _need(k_rope, "k_rope", bf, (B, S, dr))
+    _need(v, "v", bf, (B, S, H, dv_))
+    _need(out, "out", bf, (B, S, H, dv_))
+    _need(lse, "lse", torch.float32, (B, H, S))
+    _need(d_out, "d_out", bf, (B, S, H, dv_))
+    dev = q_nope.device
+    if grads is None:
+        grads = (torch.empty((B, S, H, dn), dtype=bf, device=dev),
+                 torch.empty((B, S, H, dr), dtype=bf, device=dev),
+                 torch.empty((B, S, H, dn), dtype=bf, device=dev),
+                 torch.empty((B, S, dr), dtype=torch.float32, device=dev),
+                 torch.empty((B, S, H, dv_), dtype=bf, device=dev))
+    dq_n, dq_r, dk_n, dk_r, dv = grads
+    _need(dq_n, "dq_nope", bf, (B, S, H, dn))
+    _need(dq_r, "dq_rope", bf, (B, S, H, dr))
+    _need(dk_n, "dk_nope", bf, (B, S, H, dn))
+    _need(dk_r, "dk_rope", torch.float32, (B, S, dr))
+    _need(dv, "dv", bf, (B, S, H, dv_))
+    need = prefill_backward_workspace_size(B, H, S)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    st = _lib.mla_prefill_backward(_ptr(q_nope), _ptr(q_rope), _ptr(k_nope), _ptr(k_rope), _ptr(v),
+                                   _ptr(out), _ptr(lse), _ptr(d_out), _ptr(dq_n), _ptr(dq_r),
+                                   _ptr(dk_n), _ptr(dk_r), _ptr(dv), B, H, S, dn, dr, dv_,
+                                   float(softmax_scale), int(bool(causal)), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st)
+    return dq_n, dq_r, dk_n, dk_r, dv
 
 
 def decode_workspace_size(B: int, H: int, q_len: int, d_latent: int = 512) -> int:

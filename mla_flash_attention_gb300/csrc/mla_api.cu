@@ -32,6 +32,13 @@ cudaError_t launch_decode_combine(const float* part_o, const float* part_lse,
                                   int T, int max_pages, int G, cudaStream_t stream);
 cudaError_t launch_absorb_sm103(const void* x, const void* w, void* y, int R, int H, int K, int N,
                                 unsigned int* err, cudaStream_t stream);
+size_t prefill_bwd_workspace_bytes(int B, int H, int S);
+cudaError_t launch_prefill_bwd_sm103(const void* q_nope, const void* q_rope, const void* k_nope,
+                                     const void* k_rope, const void* v, const void* out,
+                                     const float* lse, const void* d_out, void* dq_nope,
+                                     void* dq_rope, void* dk_nope, float* dk_rope, void* dv,
+                                     int B, int H, int S, float softmax_scale, int causal,
+                                     void* workspace, unsigned int* err, cudaStream_t stream);
 cudaError_t launch_cache_append(const void* c_new, void* cache, float* kv_scale,
                                 const int* page_table, const int* cache_lens, int B, int T,
                                 int max_pages, int num_pages, bool fp8, unsigned int* err,
@@ -188,6 +195,50 @@ mla_status mla_prefill(const void* q_nope, const void* q_rope, const void* k_nop
                                       out_dtype == MLA_FP32, err,
                                       static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "mla_prefill launch");
+  return MLA_OK;
+}
+
+size_t mla_prefill_backward_workspace_size(int B, int H, int S) {
+  if (B <= 0 || H <= 0 || S <= 0) return 0;
+  return mla::prefill_bwd_workspace_bytes(B, H, S);
+}
+
+mla_status mla_prefill_backward(const void* q_nope, const void* q_rope, const void* k_nope,
+                                const void* k_rope, const void* v, const void* out,
+                                const float* lse, const void* d_out, void* dq_nope,
+                                void* dq_rope, void* dk_nope, float* dk_rope, void* dv, int B,
+                                int H, int S, int d_nope, int d_rope, int d_v,
+                                float softmax_scale, int causal, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  if (!q_nope || !q_rope || !k_nope || !k_rope || !v || !out || !lse || !d_out || !dq_nope ||
+      !dq_rope || !dk_nope || !dk_rope || !dv)
+    return fail(MLA_ERR_INVALID_ARG, "mla_prefill_backward: null tensor pointer");
+  if (B <= 0 || H <= 0 || S <= 0)
+    return fail(MLA_ERR_INVALID_ARG, "mla_prefill_backward: B, H, S must be positive (got %d, %d, %d)", B, H, S);
+  if (B > 65535 || H > 65535)
+    return fail(MLA_ERR_UNSUPPORTED, "mla_prefill_backward: B and H must be at most 65535");
+  if (d_nope != 128 || d_rope != 64 || d_v != 128)
+    return fail(MLA_ERR_UNSUPPORTED, "mla_prefill_backward: only d_nope=128, d_rope=64, d_v=128 are built (got %d, %d, %d)",
+                d_nope, d_rope, d_v);
+  if (!std::isfinite(softmax_scale) || softmax_scale <= 0.f)
+    return fail(MLA_ERR_INVALID_ARG, "mla_prefill_backward: softmax_scale must be finite and positive");
+  const void* ptrs[] = {q_nope, q_rope, k_nope, k_rope, v, out, lse, d_out, dq_nope, dq_rope,
+                        dk_nope, dk_rope, dv, workspace};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return fail(MLA_ERR_INVALID_ARG, "mla_prefill_backward: tensors must be 16-byte aligned");
+  if ((double)B * S * H * 128 >= 9.0e18 || 2.0 * B * H * ((S + 127) / 128) > 2147483647.0)
+    return fail(MLA_ERR_UNSUPPORTED, "mla_prefill_backward: problem too large");
+  const size_t need = mla::prefill_bwd_workspace_bytes(B, H, S);
+  if (!workspace || workspace_bytes < need)
+    return fail(MLA_ERR_WORKSPACE, "mla_prefill_backward: workspace of %zu bytes is smaller than the %zu needed",
+                workspace_bytes, need);
+  unsigned int* err = device_error_word();
+  if (!err) return fail(MLA_ERR_CUDA, "mla_prefill_backward: device error word not reachable");
+  cudaError_t e = mla::launch_prefill_bwd_sm103(q_nope, q_rope, k_nope, k_rope, v, out, lse, d_out,
+                                                dq_nope, dq_rope, dk_nope, dk_rope, dv, B, H, S,
+                                                softmax_scale, causal != 0, workspace, err,
+                                                static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mla_prefill_backward launch");
   return MLA_OK;
 }
 

@@ -95,3 +95,31 @@ def test_decode_argument_checks(clib):
     assert _decode(clib, ks=16) == 1           # bf16 with scales
     assert _decode(clib, out=8) == 1           # misaligned
     assert _decode(clib, npages=0) == 1
+
+
+def _backward(clib, **kw):
+    names = ("qn", "qr", "kn", "kr", "v", "out", "lse", "do", "dqn", "dqr", "dkn", "dkr", "dv")
+    a = {n: 16 for n in names}
+    a.update(B=1, H=1, S=1, dn=128, dr=64, dvd=128, scale=0.1, causal=1, ws=None, wsb=0)
+    a.update(kw)
+    f = clib.mla_prefill_backward
+    f.restype = ctypes.c_int
+    P = ctypes.c_void_p
+    return f(*[P(a[n]) for n in names], a["B"], a["H"], a["S"], a["dn"], a["dr"], a["dvd"],
+             ctypes.c_float(a["scale"]), a["causal"], P(a["ws"]), ctypes.c_size_t(a["wsb"]), None)
+
+
+def test_backward_argument_checks(clib):
+    clib.mla_prefill_backward_workspace_size.restype = ctypes.c_size_t
+    need = clib.mla_prefill_backward_workspace_size(2, 3, 300)
+    assert need == 2 * ((2 * 3 * 384 * 4 + 255) // 256 * 256)
+    assert clib.mla_prefill_backward_workspace_size(0, 3, 300) == 0
+    assert _backward(clib, do=None) == 1
+    assert _backward(clib, dkr=None) == 1
+    assert _backward(clib, S=0) == 1
+    assert _backward(clib, dn=64) == 2
+    assert _backward(clib, dvd=512) == 2
+    assert _backward(clib, dqr=40) == 1          # misaligned
+    assert _backward(clib, scale=-1.0) == 1
+    assert _backward(clib) == 3                  # no workspace
+    assert _backward(clib, ws=16, wsb=100) == 3  # workspace too small
