@@ -8,19 +8,19 @@
 //
 // Two CTA roles share one launch, one kernel body and one shared-memory plan:
 //   key-tile CTAs (b, h, 128 keys): K and V stay in shared memory; query tiles stream by.
-//     TMEM: X [0,128)  S' = K Q' (keys on lanes), then dP' = V dO', then dS' (bf16 pairs)
-//           dV [128,256), dK [256,448) (nope 128 + rope 64), Y [448,512) P' (bf16 pairs)
-//     MMAs per query tile: S' (SS), dP' (SS), dV += P' dO (TS: A = Y), dK += dS' Q (TS: A = X)
+//     TMEM: X [0,128) S' = K Q' (keys on lanes), then dP' = V dO'; dV [128,256);
+//           dK [256,448) (nope 128 + rope 64); Y [448,512) P', then dS' (bf16 pairs)
+//     MMAs per query tile n: dP'(n), dV += P' dO (TS: A = Y), S'(n+1), dK += dS' Q (TS: A = Y)
 //   query-tile CTAs (b, h, 128 queries): Q and dO stay; key tiles stream by.
-//     TMEM: X [0,128) S = Q K', then dS (bf16 pairs); [128,256) dP = dO V'; dQ [256,448)
-//     MMAs per key tile: S (SS), dP (SS), dQ += dS K (TS: A = X)
+//     TMEM: X [0,128) S = Q K'; [128,256) dP = dO V'; dQ [256,448); Y [448,512) dS (bf16)
+//     MMAs per key tile n: S(n+1), dQ += dS K (TS: A = Y), dP(n+1)
+//   Scores of the next tile are issued as soon as the elementwise warps have read the
+//   current ones out of X, so the tensor pipe works while the exponentials are computed.
 // Shared memory (both roles): fixed 3-chunk tile (K | Q) + fixed 2-chunk tile (V | dO), a
 // 2-stage ring of streamed 3-chunk tiles (Q | K), one streamed 2-chunk tile (dO | V), and
 // the streamed query tiles' -LSE*log2(e) and D vectors (key-tile role).
 // Warps: 0 TMA producer, 1 MMA issuer, 2-9 elementwise (TMEM lane quarter = warp % 4,
-// column half = (warp - 2) / 4).  Each column half writes its bf16 dS into the first 32
-// columns of the 64 fp32 columns it has just read, so no half overwrites values the other
-// half still has to read.
+// column half = (warp - 2) / 4; each half owns 64 score columns and 32 packed columns of Y).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -57,7 +57,7 @@ struct Params {
 
 struct Bars {
   uint64_t fix_full, ring_full[2], ring_empty[2], one_full, one_empty;
-  uint64_t s_full, x_read, dp_full, p_ready, dv_done, ds_ready, acc_done;
+  uint64_t s_full, x_read, dp_full, dp_read, p_ready, dv_done, ds_ready, acc_step, acc_done;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -159,7 +159,29 @@ __device__ __forceinline__ void bwd_body(const Maps& m, const Params& p, unsigne
         ptx::tma_load_4d(f2_, m.dout, &bars.fix_full, 0, h, row0, b);
         ptx::tma_load_4d(f2_ + kChunk, m.dout, &bars.fix_full, 64, h, row0, b);
       }
+      constexpr int kAhead = 2;  // tiles warmed in L2 ahead of their load
+      auto warm = [&](int n) {
+        const int r0 = (t_begin + n) * BT;
+        if (kKeyRole) {
+          ptx::tma_prefetch_4d(m.qn, 0, h, r0, b);
+          ptx::tma_prefetch_4d(m.qn, 64, h, r0, b);
+          ptx::tma_prefetch_4d(m.qr, 0, h, r0, b);
+          ptx::tma_prefetch_4d(m.dout, 0, h, r0, b);
+          ptx::tma_prefetch_4d(m.dout, 64, h, r0, b);
+          const size_t vo = (size_t)bh * p.S_pad + r0;
+          ptx::bulk_prefetch(p.nlse2 + vo, BT * 4);
+          ptx::bulk_prefetch(p.dvec + vo, BT * 4);
+        } else {
+          ptx::tma_prefetch_4d(m.kn, 0, h, r0, b);
+          ptx::tma_prefetch_4d(m.kn, 64, h, r0, b);
+          ptx::tma_prefetch_3d(m.kr, 0, r0, b);
+          ptx::tma_prefetch_4d(m.v, 0, h, r0, b);
+          ptx::tma_prefetch_4d(m.v, 64, h, r0, b);
+        }
+      };
+      for (int n = 0; n < kAhead && n < nsteps; ++n) warm(n);
       for (int n = 0; n < nsteps; ++n) {
+        if (n + kAhead < nsteps) warm(n + kAhead);
         const int r0 = (t_begin + n) * BT, s = n & 1;
         if (!ptx::mbar_wait(&bars.ring_empty[s], ((n >> 1) & 1) ^ 1, abort_flag, p.err)) break;
         unsigned char* dst = sm + kOffRing + s * 3 * kChunk;
@@ -195,13 +217,12 @@ __device__ __forceinline__ void bwd_body(const Maps& m, const Params& p, unsigne
       constexpr uint32_t kIdAcc = ptx::make_idesc(1, BT, 192, 0, 1);  // B N-major, N = 192
       const uint32_t base = ptx::smem_u32(sm);
       const uint32_t one = base + kOffOne;
-      bool ok = ptx::mbar_wait(&bars.fix_full, 0, abort_flag, p.err);
-      for (int n = 0; ok && n < nsteps; ++n) {
-        const int s = n & 1;
-        if (!(ok = ptx::mbar_wait(&bars.ring_full[s], (n >> 1) & 1, abort_flag, p.err))) break;
+      auto ring_of = [&](int n) { return base + kOffRing + (n & 1) * 3 * kChunk; };
+      // scores over the 192-deep nope+rope contraction (key role: transposed, keys on lanes)
+      auto issue_s = [&](int n) -> bool {
+        if (!ptx::mbar_wait(&bars.ring_full[n & 1], (n >> 1) & 1, abort_flag, p.err)) return false;
         ptx::tc_fence_after();
-        const uint32_t ring = base + kOffRing + s * 3 * kChunk;
-        // scores over the 192-deep nope+rope contraction (key role: transposed, keys on lanes)
+        const uint32_t ring = ring_of(n);
 #pragma unroll
         for (int k = 0; k < 12; ++k) {
           const uint32_t off = (k >> 2) * kChunk + (k & 3) * 32;
@@ -209,13 +230,12 @@ __device__ __forceinline__ void bwd_body(const Maps& m, const Params& p, unsigne
                            ptx::sw128_desc(ring + off, 16, 1024), kIdS, k > 0);
         }
         ptx::mma_commit(&bars.s_full);
-        if (kKeyRole) {  // dP' reuses X once the scores have been read out
-          if (!(ok = ptx::mbar_wait(&bars.x_read, n & 1, abort_flag, p.err))) break;
-          ptx::tc_fence_after();
-        }
-        if (!(ok = ptx::mbar_wait(&bars.one_full, n & 1, abort_flag, p.err))) break;
+        return true;
+      };
+      // dP = dO V' over d_v = 128 (key role: dP' = V dO' into X; query role: own columns)
+      auto issue_dp = [&](int n) -> bool {
+        if (!ptx::mbar_wait(&bars.one_full, n & 1, abort_flag, p.err)) return false;
         ptx::tc_fence_after();
-        // dP = dO V' over d_v = 128 (key role: dP' = V dO')
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t off = (k >> 2) * kChunk + (k & 3) * 32;
@@ -224,28 +244,55 @@ __device__ __forceinline__ void bwd_body(const Maps& m, const Params& p, unsigne
                            ptx::sw128_desc(one + off, 16, 1024), kIdS, k > 0);
         }
         ptx::mma_commit(&bars.dp_full);
-        if (kKeyRole) {
-          // dV += P' dO: A = P' (bf16 pairs in Y), B = the streamed dO tile, N-major
-          if (!(ok = ptx::mbar_wait(&bars.p_ready, n & 1, abort_flag, p.err))) break;
-          ptx::tc_fence_after();
+        return true;
+      };
+      // dK += dS' Q (key role) or dQ += dS K: A = dS (bf16 pairs in Y), B = the streamed
+      // 192-wide tile, N-major
+      auto issue_acc = [&](int n) {
+        const uint32_t ring = ring_of(n);
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
+        for (int k = 0; k < 8; ++k)
+          ptx::mma_bf16_ts(tmem + kColAcc, tmem + kColY + k * 8,
+                           ptx::sw128_desc(ring + k * 2048, kChunk, 1024), kIdAcc,
+                           (n > 0 || k > 0) ? 1u : 0u);
+        ptx::mma_commit(&bars.ring_empty[n & 1]);
+        ptx::mma_commit(&bars.acc_step);
+      };
+      auto wait = [&](uint64_t* bar, int n) -> bool {
+        if (!ptx::mbar_wait(bar, n & 1, abort_flag, p.err)) return false;
+        ptx::tc_fence_after();
+        return true;
+      };
+      bool ok = ptx::mbar_wait(&bars.fix_full, 0, abort_flag, p.err) && issue_s(0);
+      if (kKeyRole) {
+        // per query tile n: dP'(n) | dV(n) | S'(n+1) | dK(n) -- the next scores run while the
+        // elementwise warps turn dP'(n) into dS(n)
+        for (int n = 0; ok && n < nsteps; ++n) {
+          if (!(ok = wait(&bars.x_read, n) && issue_dp(n))) break;
+          if (!(ok = wait(&bars.p_ready, n))) break;
+#pragma unroll
+          for (int k = 0; k < 8; ++k)  // dV += P' dO: A = P' (bf16 pairs in Y), B = dO N-major
             ptx::mma_bf16_ts(tmem + kColDV, tmem + kColY + k * 8,
                              ptx::sw128_desc(one + k * 2048, kChunk, 1024), kIdDV,
                              (n > 0 || k > 0) ? 1u : 0u);
           ptx::mma_commit(&bars.dv_done);
+          ptx::mma_commit(&bars.one_empty);
+          if (n + 1 < nsteps && !(ok = wait(&bars.dp_read, n) && issue_s(n + 1))) break;
+          if (!(ok = wait(&bars.ds_ready, n))) break;
+          issue_acc(n);
         }
-        ptx::mma_commit(&bars.one_empty);
-        // dK += dS' Q (key role) or dQ += dS K: A = dS (bf16 pairs in the first 32 columns
-        // of each 64-column half of X), B = the streamed 192-wide tile, N-major
-        if (!(ok = ptx::mbar_wait(&bars.ds_ready, n & 1, abort_flag, p.err))) break;
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          ptx::mma_bf16_ts(tmem + kColAcc, tmem + kColX + (k >> 2) * 64 + (k & 3) * 8,
-                           ptx::sw128_desc(ring + k * 2048, kChunk, 1024), kIdAcc,
-                           (n > 0 || k > 0) ? 1u : 0u);
-        ptx::mma_commit(&bars.ring_empty[s]);
+      } else {
+        // per key tile n: S(n+1) | dQ(n) | dP(n+1), with dP(0) issued up front
+        if (ok && (ok = issue_dp(0))) ptx::mma_commit(&bars.one_empty);
+        for (int n = 0; ok && n < nsteps; ++n) {
+          if (n + 1 < nsteps && !(ok = wait(&bars.x_read, n) && issue_s(n + 1))) break;
+          if (!(ok = wait(&bars.ds_ready, n))) break;
+          issue_acc(n);
+          if (n + 1 < nsteps) {
+            if (!(ok = wait(&bars.dp_read, n) && issue_dp(n + 1))) break;
+            ptx::mma_commit(&bars.one_empty);
+          }
+        }
       }
       if (ok) ptx::mma_commit(&bars.acc_done);
     }
@@ -265,25 +312,31 @@ __device__ __forceinline__ void bwd_body(const Maps& m, const Params& p, unsigne
       d_row = p.dvec[(size_t)bh * p.S_pad + row_idx];
     }
     const uint64_t sc2 = ptx::f2(p.scale_log2, p.scale_log2);
+    // all lanes wait (bounded); the warp goes on only if every lane saw the phase
+    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      const bool w = __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, abort_flag, p.err));
+      if (w) ptx::tc_fence_after();
+      return w;
+    };
+    // one arrival per warp once its TMEM reads / writes are complete
+    auto arrive = [&](uint64_t* bar) {
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar);
+    };
     bool ok = true;
     for (int n = 0; n < nsteps; ++n) {
       const int t = t_begin + n, s = n & 1;
       const float* vec = reinterpret_cast<const float*>(sm + kOffVec + s * 2 * BT * 4);
-      ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.s_full, n & 1, abort_flag, p.err));
+      ok = wait(&bars.s_full, n & 1);
       // the query vectors of this stage arrived with its TMA transaction: observe it directly
-      if (kKeyRole && ok)
-        ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.ring_full[s], (n >> 1) & 1, abort_flag, p.err));
+      if (kKeyRole && ok) ok = wait(&bars.ring_full[s], (n >> 1) & 1);
       if (!ok) break;
-      ptx::tc_fence_after();
       uint32_t u[64];
       ptx::tmem_ld32(tX, *reinterpret_cast<uint32_t(*)[32]>(u));
       ptx::tmem_ld32(tX + 32, *reinterpret_cast<uint32_t(*)[32]>(u + 32));
       ptx::tmem_ld_wait();
-      if (kKeyRole) {
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&bars.x_read);
-      }
+      arrive(&bars.x_read);
       // P = exp2(s * scale * log2(e) - LSE * log2(e)), two columns per packed instruction
       float pr[64];
       if (kKeyRole) {
@@ -323,26 +376,20 @@ __device__ __forceinline__ void bwd_body(const Maps& m, const Params& p, unsigne
       }
       uint32_t pk[32];
       if (kKeyRole) {
-        // P' (bf16) into Y once the previous dV product has consumed it
-        if (n > 0) {
-          ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.dv_done, (n - 1) & 1, abort_flag, p.err));
-          if (!ok) break;
-        }
+        // P' (bf16) into Y once dK(n-1) has consumed the dS' held there
+        if (n > 0 && !(ok = wait(&bars.acc_step, (n - 1) & 1))) break;
 #pragma unroll
         for (int x = 0; x < 32; ++x) pk[x] = ptx::pack_bf16x2(pr[2 * x], pr[2 * x + 1]);
         ptx::tmem_st32(tY, pk);
         ptx::tmem_st_wait();
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&bars.p_ready);
+        arrive(&bars.p_ready);
       }
-      ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.dp_full, n & 1, abort_flag, p.err));
-      if (!ok) break;
-      ptx::tc_fence_after();
+      if (!(ok = wait(&bars.dp_full, n & 1))) break;
       ptx::tmem_ld32(tDP, *reinterpret_cast<uint32_t(*)[32]>(u));
       ptx::tmem_ld32(tDP + 32, *reinterpret_cast<uint32_t(*)[32]>(u + 32));
       ptx::tmem_ld_wait();
-      // dS = P * (dP - D), rounded to bf16 pairs over the first 32 columns just read
+      arrive(&bars.dp_read);
+      // dS = P * (dP - D) as bf16 pairs
       if (kKeyRole) {
         const float2* dd = reinterpret_cast<const float2*>(vec + BT) + hf * 32;  // per query
 #pragma unroll
@@ -362,11 +409,16 @@ __device__ __forceinline__ void bwd_body(const Maps& m, const Params& p, unsigne
           pk[x] = ptx::pack_bf16x2(ptx::f2_lo(g), ptx::f2_hi(g));
         }
       }
-      ptx::tmem_st32(tX, pk);
+      // dS into Y once its previous reader is done: dV(n) (key role: P' lives there) or
+      // dQ(n-1)
+      if (kKeyRole) {
+        if (!(ok = wait(&bars.dv_done, n & 1))) break;
+      } else if (n > 0 && !(ok = wait(&bars.acc_step, (n - 1) & 1))) {
+        break;
+      }
+      ptx::tmem_st32(tY, pk);
       ptx::tmem_st_wait();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&bars.ds_ready);
+      arrive(&bars.ds_ready);
     }
     // ---------------------------------------------------------------- epilogue
     if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.acc_done, 0, abort_flag, p.err));
@@ -431,12 +483,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   __shared__ Bars bars;
   const int warp = threadIdx.x >> 5;
-  const int BH = p.B * p.H;
-  // key-tile CTAs first (most query tiles first), then query-tile CTAs (most key tiles first)
+  // key-tile CTAs first, then query-tile CTAs; within a role the tiles of one (b, h) are
+  // consecutive (most work first), so CTAs that run together stream the same (b, h)'s tiles
+  // and find them in L2
   const bool key_role = static_cast<int>(blockIdx.x) < p.n_key_ctas;
   const int idx = key_role ? blockIdx.x : blockIdx.x - p.n_key_ctas;
-  const int tile = key_role ? idx / BH : p.nt - 1 - idx / BH;
-  const int bh = idx % BH;
+  const int bh = idx / p.nt;
+  const int tile = key_role ? idx % p.nt : p.nt - 1 - idx % p.nt;
   const int b = bh / p.H, h = bh % p.H;
 
   if (threadIdx.x == 0) {
@@ -451,6 +504,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(&bars.s_full, 1);
     ptx::mbar_init(&bars.x_read, 8);    // one arrival per elementwise warp
     ptx::mbar_init(&bars.dp_full, 1);
+    ptx::mbar_init(&bars.dp_read, 8);
+    ptx::mbar_init(&bars.acc_step, 1);
     ptx::mbar_init(&bars.p_ready, 8);
     ptx::mbar_init(&bars.dv_done, 1);
     ptx::mbar_init(&bars.ds_ready, 8);
