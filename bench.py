@@ -394,10 +394,10 @@ def run_gpu(args):
                 "tflops": world * tf, "frac_bf16_peak": tf / pk["bf16_tflops"],
                 "flop_per_pair": 2 * (192 + 128 + 128 + 192 + 192),
                 "issued_flop_per_pair": 2 * (2 * 192 + 2 * 128 + 128 + 192 + 192),
-                "l2": "inputs (2.7 GB) larger than L2; no flush", "launches_per_call": 2}
+                "l2": "inputs (2.7 GB) larger than L2; no flush", "launches_per_call": 3}
 
     res["prefill_backward"] = backward_entry()
-    launches += args.steps * 2
+    launches += args.steps * 3  # prep, zero fill, main
     torch.cuda.empty_cache()
 
     def chunked_entry():

@@ -48,7 +48,7 @@ struct Params {
   uint16_t* dq_nope;   // [B, S, H, 128]
   uint16_t* dq_rope;   // [B, S, H, 64]
   uint16_t* dk_nope;   // [B, S, H, 128]
-  float* dk_rope;      // [B, S, 64], accumulated (zeroed by the prep kernel)
+  float* dk_rope;      // [B, S, 64], accumulated (zeroed before the launch)
   uint16_t* dv;        // [B, S, H, 128]
   unsigned int* err;
   int B, H, S, S_pad, nt, causal, n_key_ctas;
@@ -62,48 +62,69 @@ struct Bars {
   int abort_flag;
 };
 
-// D = rowsum(dO * O) and -LSE*log2(e) per (b, h, query) into padded [B*H, S_pad] vectors,
-// and zero the rope-key gradient accumulator.  One warp per (b, query, h) row.
+// D = rowsum(dO * O) and -LSE*log2(e) per (b, h, query) into padded [B*H, S_pad] vectors.
+// One warp per (b, h, 32 consecutive queries): each 256-byte row of dO and O is read by the
+// whole warp (8 bytes a lane), the 32 per-lane partial sums are reduced across lanes by a
+// transposing butterfly (16 + 8 + 4 + 2 + 1 exchanges) that leaves row i0 + lane's sum in
+// lane `lane`, so the D and LSE accesses are 128-byte coalesced.
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restrict__ out,
                                                        const uint16_t* __restrict__ d_out,
                                                        const float* __restrict__ lse,
                                                        float* __restrict__ nlse2,
-                                                       float* __restrict__ dvec,
-                                                       float* __restrict__ dk_rope, int B, int H,
+                                                       float* __restrict__ dvec, int B, int H,
                                                        int S, int S_pad) {
-  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const long long task = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (row >= (long long)B * S_pad * H) return;
-  const int h = static_cast<int>(row % H);
-  const long long bi = row / H;
-  const int i = static_cast<int>(bi % S_pad), b = static_cast<int>(bi / S_pad);
-  const size_t vo = ((size_t)b * H + h) * S_pad + i;
-  if (i >= S) {
-    if (lane == 0) {
-      nlse2[vo] = -INFINITY;
-      dvec[vo] = 0.f;
-    }
-    return;
-  }
-  const size_t ro = (((size_t)b * S + i) * H + h) * 128 + lane * 4;
-  const uint2 a = *reinterpret_cast<const uint2*>(d_out + ro);
-  const uint2 o = *reinterpret_cast<const uint2*>(out + ro);
+  const int groups = S_pad / 32;
+  if (task >= (long long)B * H * groups) return;
+  const int g = static_cast<int>(task % groups);
+  const int bh = static_cast<int>(task / groups);
+  const int b = bh / H, h = bh % H;
+  const int i0 = g * 32;
   auto lo = [](uint32_t w) { return __uint_as_float(w << 16); };
   auto hi = [](uint32_t w) { return __uint_as_float(w & 0xffff0000u); };
-  float acc = lo(a.x) * lo(o.x);
-  acc = fmaf(hi(a.x), hi(o.x), acc);
-  acc = fmaf(lo(a.y), lo(o.y), acc);
-  acc = fmaf(hi(a.y), hi(o.y), acc);
+  float part[32];
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) {
-    dvec[vo] = acc;
-    nlse2[vo] = -lse[((size_t)b * H + h) * S + i] * 1.4426950408889634f;
+  for (int r = 0; r < 32; ++r) {
+    part[r] = 0.f;
+    if (i0 + r < S) {
+      const size_t ro = (((size_t)b * S + i0 + r) * H + h) * 128 + lane * 4;
+      const uint2 a = __ldg(reinterpret_cast<const uint2*>(d_out + ro));
+      const uint2 o = __ldg(reinterpret_cast<const uint2*>(out + ro));
+      float acc = lo(a.x) * lo(o.x);
+      acc = fmaf(hi(a.x), hi(o.x), acc);
+      acc = fmaf(lo(a.y), lo(o.y), acc);
+      part[r] = fmaf(hi(a.y), hi(o.y), acc);
+    }
   }
-  if (h == 0) {
-    float2* z = reinterpret_cast<float2*>(dk_rope + ((size_t)b * S + i) * 64) + lane;
-    *z = make_float2(0.f, 0.f);
+  // after the round with offset w, part[0 .. w) of lane l hold partial sums of rows
+  // (l & ~(2w-1) & 31) ... ; at the end part[0] of lane l is the full sum of row l
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool upper = (lane & w) != 0;
+#pragma unroll
+    for (int r = 0; r < w; ++r) {
+      const float send = upper ? part[r] : part[r + w];
+      const float keep = upper ? part[r + w] : part[r];
+      part[r] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+    }
   }
+  const int i = i0 + lane;
+  const size_t vo = (size_t)bh * S_pad + i;
+  if (i < S) {
+    dvec[vo] = part[0];
+    nlse2[vo] = -lse[(size_t)bh * S + i] * 1.4426950408889634f;
+  } else {
+    dvec[vo] = 0.f;
+    nlse2[vo] = -INFINITY;
+  }
+}
+
+// Zero the rope-key gradient accumulator (n4 float4 stores).
+__global__ void __launch_bounds__(256) bwd_zero_kernel(float4* __restrict__ p, long long n4) {
+  for (long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x; k < n4;
+       k += (long long)gridDim.x * blockDim.x)
+    p[k] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // 32 fp32 accumulator columns (times `mul`) -> 32 bf16 at dst (64 bytes, 16-byte aligned)
@@ -565,12 +586,14 @@ cudaError_t launch_prefill_bwd_sm103(const void* q_nope, const void* q_rope, con
   float* nlse2 = static_cast<float*>(workspace);
   float* dvec = reinterpret_cast<float*>(static_cast<char*>(workspace) + vec);
 
-  const long long rows = (long long)B * S_pad * H;
-  const long long prep_blocks = (rows + 7) / 8;
+  const long long tasks = (long long)B * H * (S_pad / 32);
+  const long long prep_blocks = (tasks + 7) / 8;
   if (prep_blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   bwd_prep_kernel<<<(unsigned)prep_blocks, 256, 0, stream>>>(
-      static_cast<const uint16_t*>(out), static_cast<const uint16_t*>(d_out), lse, nlse2, dvec,
-      dk_rope, B, H, S, S_pad);
+      static_cast<const uint16_t*>(out), static_cast<const uint16_t*>(d_out), lse, nlse2, dvec, B,
+      H, S, S_pad);
+  bwd_zero_kernel<<<1024, 256, 0, stream>>>(reinterpret_cast<float4*>(dk_rope),
+                                            (long long)B * S * 64 / 4);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
