@@ -150,13 +150,8 @@ cudaError_t launch_absorb_sm103(const void* x, const void* w, void* y, int R, in
   if ((e = encode_tensor_map(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, x, xd, xs, xb)) != cudaSuccess ||
       (e = encode_tensor_map(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w, wd, ws, wb)) != cudaSuccess)
     return e;
-  static bool ready = false;
-  if (!ready) {
-    if ((e = cudaFuncSetAttribute(absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  kSmemAlloc)) != cudaSuccess)
-      return e;
-    ready = true;
-  }
+  static unsigned long long smem_set = 0;
+  if ((e = smem_attr_once(absorb_kernel, kSmemAlloc, &smem_set)) != cudaSuccess) return e;
   Params p;
   p.y = static_cast<uint16_t*>(y);
   p.err = err;

@@ -627,13 +627,8 @@ cudaError_t launch_prefill_bwd_sm103(const void* q_nope, const void* q_rope, con
   const long long per_role = (long long)B * H * nt;
   if (2 * per_role > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   p.n_key_ctas = (int)per_role;
-  static bool attr_set = false;
-  if (!attr_set) {
-    e = cudaFuncSetAttribute(prefill_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemAlloc);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static unsigned long long smem_set = 0;
+  if ((e = smem_attr_once(prefill_bwd_kernel, kSmemAlloc, &smem_set)) != cudaSuccess) return e;
   prefill_bwd_kernel<<<(unsigned)(2 * per_role), kThreads, kSmemAlloc, stream>>>(tqn, tqr, tkn,
                                                                                   tkr, tv, tdo, p);
   return cudaGetLastError();

@@ -39,4 +39,19 @@ __device__ __forceinline__ int pages_of(int L, int page_size) {
 // unit c for sequence b goes to slot c + b, which is unique because consecutive units
 // never move backwards through the sequences; there are at most G + B - 1 slots.
 
+// Opt `kernel` into `bytes` of dynamic shared memory on the current device.  The attribute
+// belongs to the device, so it is set once per device ordinal: `done` holds one bit per
+// ordinal below 64 (higher ordinals set it on every call).
+template <typename Kernel>
+inline cudaError_t smem_attr_once(Kernel kernel, int bytes, unsigned long long* done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (__atomic_load_n(done, __ATOMIC_ACQUIRE) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) __atomic_fetch_or(done, bit, __ATOMIC_ACQ_REL);
+  return e;
+}
+
 }  // namespace mla

@@ -685,13 +685,9 @@ cudaError_t launch_decode_sm103(const void* q_latent, const void* q_rope, const 
   p.G = G;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   auto go = [&](auto kern) -> cudaError_t {
-    static bool checked[2] = {false, false};
-    if (!checked[fp8 ? 1 : 0]) {
-
-      cudaError_t e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
-      if (e2 != cudaSuccess) return e2;
-      checked[fp8 ? 1 : 0] = true;
-    }
+    static unsigned long long smem_set[2] = {0, 0};
+    const cudaError_t e2 = smem_attr_once(kern, kSmemAlloc, &smem_set[fp8 ? 1 : 0]);
+    if (e2 != cudaSuccess) return e2;
     kern<<<2 * G, fp8 ? kThreadsOf<true> : kThreadsOf<false>, kSmemAlloc, stream>>>(tm, tm_qlat, tm_qrope, p);
     return cudaGetLastError();
   };

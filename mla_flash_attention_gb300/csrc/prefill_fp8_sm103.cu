@@ -429,13 +429,8 @@ cudaError_t launch_prefill_sm103_fp8(const void* q_nope, const void* q_rope, con
   p.out = out;
   p.lse = lse;
   p.err = err;
-  static bool ready = false;
-  if (!ready) {
-    if ((e = cudaFuncSetAttribute(prefill_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  kSmemAlloc)) != cudaSuccess)
-      return e;
-    ready = true;
-  }
+  static unsigned long long smem_set = 0;
+  if ((e = smem_attr_once(prefill_fp8_kernel, kSmemAlloc, &smem_set)) != cudaSuccess) return e;
   const long long grid = (long long)B * H * p.nrb;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   prefill_fp8_kernel<<<(unsigned)grid, kThreads, kSmemAlloc, stream>>>(tqn, tqr, tkn, tkr, tv, p);

@@ -420,18 +420,20 @@ cudaError_t launch_prefill_sm103_bf16(const void* q_nope, const void* q_rope, co
   p.out = out;
   p.lse = lse;
   p.err = err;
-  static bool attr_set = false;
-  if (!attr_set) {
-    // The warpgroups trade registers at run time (setmaxnreg): 128 threads drop to 56 and
-    // 256 rise to 224, which needs exactly 168 per thread at launch.  Refuse otherwise.
+  // The warpgroups trade registers at run time (setmaxnreg): 128 threads drop to 56 and 256
+  // rise to 224, which needs exactly 168 per thread at launch.  Refuse otherwise.
+  static int regs_ok = 0;  // 0 unknown, 1 checked
+  if (!__atomic_load_n(&regs_ok, __ATOMIC_ACQUIRE)) {
     cudaFuncAttributes fa;
     cudaError_t e = cudaFuncGetAttributes(&fa, prefill_bf16_kernel);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != 168) return cudaErrorInvalidDeviceFunction;
-    e = cudaFuncSetAttribute(prefill_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemAlloc);
+    __atomic_store_n(&regs_ok, 1, __ATOMIC_RELEASE);
+  }
+  static unsigned long long smem_set = 0;
+  {
+    cudaError_t e = smem_attr_once(prefill_bf16_kernel, kSmemAlloc, &smem_set);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   const long long grid = (long long)B * H * p.nrb;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
