@@ -57,25 +57,31 @@ struct Params {
   const int* page_table;
   const int* cache_lens;
   float* part_o;
-  float* part_lse;
+  float* part_lse;   // [2][n_slots][TQ]: each column half writes its own copy
+  int* counters;     // [B * NQT][2]: finished splits per (virtual sequence, half), zeroed per call
+  uint16_t* out;     // [B, T, H, 512] bf16
+  float* lse;        // [B, H, T]
   unsigned int* err;
   int B, H, T, max_pages, num_pages, causal, G;
   int NQT, TQ;  // query tiles per sequence (T*H rows in tiles of 128) and rows per tile
+  int n_slots;  // partial slots: G + B * NQT
   float scale_log2;
 };
 
 // The work unit's page range [start, end) of the flat page numbering and the first
 // sequence that reaches into it (b0, whose pages start at flat page pb0).
 struct Plan {
-  int start, end, b0, pb0;
+  int start, end, b0, pb0, chunk;
 };
 
 struct Bars {
   // stage_ready[s][k]: bf16 pages are ready at once (k = 0); fp8 pages in three parts, k = 0..2
   // covering 64-column chunks 3k..3k+2, as the in-place widening completes them
   uint64_t stage_full[kStages], stage_ready[kStages][3], stage_empty[kStages];
-  uint64_t s_full[2], p_full[2], o_done, conv_sync;
+  uint64_t s_full[2], p_full[2], o_done, seg_done, conv_sync;
   uint64_t q_free, q_lo_full, q_cp_done, q_hi_full;  // per-sequence Q staging
+  uint64_t part_done, merge_go;  // partial written by the 4 softmax warps / merge decision
+  int merge_last;
   uint32_t tmem_base;
   int abort_flag;
   Plan plan;
@@ -139,7 +145,7 @@ __device__ void make_plan(const Params& prm, int unit, Plan* out) {
       }
     }
   }
-  if (lane == 0) *out = Plan{start, end, b0, pb0};
+  if (lane == 0) *out = Plan{start, end, b0, pb0, chunk};
 }
 
 // Walks the (sequence, page range) segments of this CTA's work unit in order; every
@@ -158,9 +164,10 @@ struct Segments {
     pb = plan.pb0;
   }
   // Next non-empty segment: sets seq (the virtual sequence: sequence * NQT + query tile),
-  // L, lo, hi (page indices within the sequence).
+  // L, lo, hi (page indices within the sequence); flat0 = the sequence's first flat page.
   // Lengths are fetched eight at a time so that skipping to this unit's first sequence
   // costs one load latency per eight sequences rather than one per sequence.
+  int flat0 = 0;
   __device__ bool next(int& seq, int& L, int& lo, int& hi) {
     while (b < B && pb < end) {
       int Ls[8];
@@ -172,10 +179,11 @@ struct Segments {
         const int Lb = clamp_len(Ls[i], max_pages);
         const int n = pages_of(Lb, kPage);
         const int l0 = max(start, pb) - pb, h0 = min(end, pb + n) - pb;
-        const int cur = b;
+        const int cur = b, cur_pb = pb;
         pb += n;
         ++b;
         if (l0 < h0) {
+          flat0 = cur_pb;
           seq = cur;
           L = Lb;
           lo = l0;
@@ -223,11 +231,14 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
       ptx::mbar_init(&bars.p_full[i], kRows / 32);  // one arrival per softmax warp
     }
     ptx::mbar_init(&bars.o_done, 1);
+    ptx::mbar_init(&bars.seg_done, 1);
     ptx::mbar_init(&bars.q_free, 1);
     ptx::mbar_init(&bars.q_lo_full, 1);
     ptx::mbar_init(&bars.q_cp_done, 1);
     ptx::mbar_init(&bars.q_hi_full, 1);
     ptx::mbar_init(&bars.conv_sync, kPrepThreads / 32);  // one arrival per preparation warp
+    ptx::mbar_init(&bars.part_done, kRows / 32);
+    ptx::mbar_init(&bars.merge_go, 1);
     ptx::fence_barrier_init();
   }
   // Q rows T*H..127 are never loaded: keep them zero (finite scores in the padded rows)
@@ -241,8 +252,6 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
   volatile int* abort_flag = &bars.abort_flag;
-  // the LSE combine (next launch) may be scheduled now; it waits for this grid's completion
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   Segments segs;
   segs.init(p, bars.plan);
   int seq, L, lo, hi;
@@ -395,6 +404,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
             break;
           }
         }
+        if (ok) ptx::mma_commit(&bars.seg_done);  // the segment's last PV product is complete
         g = g_end;
         ++nseg;
       }
@@ -483,8 +493,18 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
     // -------------------------------------------------------------- softmax / epilogue
     const int r = threadIdx.x - 128;  // query row == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    int g = 0;
+    int g = 0, n_epi = 0;
     bool ok = true;
+    // a sequence with no cached key is in no work unit's range: unit u writes O = 0 and
+    // LSE = -inf for the empty sequences u, u + G, u + 2G, ...
+    if (half == 0) {
+      for (int b = unit; b < p.B; b += p.G) {
+        if (clamp_len(__ldg(p.cache_lens + b), p.max_pages) > 0) continue;
+        uint4* o = reinterpret_cast<uint4*>(p.out + (size_t)b * TH * kDl);
+        for (int i = r; i < TH * (kDl / 8); i += kRows) o[i] = make_uint4(0, 0, 0, 0);
+        for (int i = r; i < TH; i += kRows) p.lse[((size_t)b * p.H + i % p.H) * p.T + i / p.H] = -INFINITY;
+      }
+    }
     while (ok && segs.next(seq, L, lo, hi)) {
       const int gr = (seq % p.NQT) * kRows + r;  // row within the sequence's T*H rows
       const int t_row = gr / p.H;
@@ -589,8 +609,13 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
         if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(&bars.p_full[g & 1]);
       }
       if (!ok) break;
-      // epilogue of the segment: partial (O_half / l, LSE) into slot unit + seq
-      ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.o_done, (g - 1) & 1, abort_flag, p.err));
+      // epilogue of the segment: partial (O_half / l, LSE) into slot unit + seq, once the
+      // segment's last PV product is complete.  That is signalled once per segment: the
+      // per-page o_done cannot be used here, since a warp that ran ahead of a slower one may
+      // arrive while PV(g-2) is still pending and one parity bit cannot tell that phase from
+      // the one after PV(g-1).  seg_done of the next segment needs this warp's P, so it is
+      // never more than one phase ahead.
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.seg_done, n_epi & 1, abort_flag, p.err));
       if (!ok) break;
       ptx::tc_fence_after();
       const size_t slot = (size_t)unit + seq;
@@ -614,9 +639,94 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
                               __uint_as_float(v[h2][4 * x + 2]) * inv, __uint_as_float(v[h2][4 * x + 3]) * inv);
         }
       }
-      if (half == 0 && r < TQ && gr < TH)
-        p.part_lse[slot * TQ + r] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+      if (r < TQ && gr < TH)
+        p.part_lse[((size_t)half * p.n_slots + slot) * TQ + r] =
+            l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
       ptx::tc_fence_before();
+      // Merge by the last split to finish: the work units that covered this virtual sequence
+      // wrote their partials of this column half into slots c + seq, c_first <= c <= c_last.
+      // Each one makes its stores visible device-wide and counts itself in; the one that
+      // completes the count (usually at the end of its unit's work) merges them:
+      // O = sum_c exp(lse_c - lse) O_c with lse = ln sum_c exp(lse_c).
+      __threadfence();
+      __syncwarp();
+      if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(&bars.part_done);
+      const int n_pages = pages_of(L, kPage);
+      const int c_first = segs.flat0 / bars.plan.chunk;
+      const int nsplit = (segs.flat0 + n_pages - 1) / bars.plan.chunk - c_first + 1;
+      if (r == 0) {
+        bool go = ptx::mbar_wait(&bars.part_done, n_epi & 1, abort_flag, p.err);
+        if (go) {
+          // the counters were zeroed by the kernel this one was launched behind
+          asm volatile("griddepcontrol.wait;" ::: "memory");
+          __threadfence();
+          const int done = atomicAdd(p.counters + (size_t)seq * 2 + half, 1) + 1;
+          __threadfence();
+          bars.merge_last = done == nsplit ? 1 : 0;
+        } else {
+          bars.merge_last = 0;
+        }
+        ptx::mbar_arrive(&bars.merge_go);
+      }
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.merge_go, n_epi & 1, abort_flag, p.err));
+      ++n_epi;
+      if (!ok) break;
+      if (*reinterpret_cast<volatile int*>(&bars.merge_last) && r < TQ && gr < TH) {
+        // this thread's row: weights of the splits from their LSEs (read through L2, in order:
+        // they were written by other SMs during this launch)
+        const float* lsp = p.part_lse + ((size_t)half * p.n_slots + c_first + seq) * TQ + r;
+        float mxl = -INFINITY;
+        for (int k = 0; k < nsplit; ++k) mxl = fmaxf(mxl, ptx::ld_l2(lsp + (size_t)k * TQ));
+        float wsum = 0.f;
+        for (int k = 0; k < nsplit; ++k) {
+          const float ls = ptx::ld_l2(lsp + (size_t)k * TQ);
+          wsum += (mxl == -INFINITY || ls == -INFINITY) ? 0.f : __expf(ls - mxl);
+        }
+        const float winv = wsum > 0.f ? 1.f / wsum : 0.f;
+        auto weight = [&](int k) -> float {
+          const float ls = ptx::ld_l2(lsp + (size_t)k * TQ);
+          return (mxl == -INFINITY || ls == -INFINITY) ? 0.f : __expf(ls - mxl) * winv;
+        };
+        const float4* src = reinterpret_cast<const float4*>(p.part_o) +
+                            ((size_t)(c_first + seq) * 128 + half * 64) * TQ + r;
+        const size_t slot_stride = (size_t)128 * TQ;
+        uint4* orow = reinterpret_cast<uint4*>(
+            p.out + ((size_t)(seq / p.NQT) * TH + gr) * kDl + half * 256);
+        // eight column quads of two splits per round: 16 independent 16-byte loads in flight
+#pragma unroll 1
+        for (int q = 0; q < 64; q += 8) {
+          float4 acc[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+          for (int k = 0; k < nsplit; k += 2) {
+            const bool two = k + 1 < nsplit;
+            float4 x0[8], x1[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              x0[j] = ptx::ld_l2(src + (size_t)k * slot_stride + (size_t)(q + j) * TQ);
+              x1[j] = two ? ptx::ld_l2(src + (size_t)(k + 1) * slot_stride + (size_t)(q + j) * TQ)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            const float w0 = weight(k), w1 = two ? weight(k + 1) : 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              acc[j].x += w0 * x0[j].x + w1 * x1[j].x;
+              acc[j].y += w0 * x0[j].y + w1 * x1[j].y;
+              acc[j].z += w0 * x0[j].z + w1 * x1[j].z;
+              acc[j].w += w0 * x0[j].w + w1 * x1[j].w;
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 8; j += 2)
+            orow[(q + j) >> 1] = make_uint4(ptx::pack_bf16x2(acc[j].x, acc[j].y), ptx::pack_bf16x2(acc[j].z, acc[j].w),
+                                            ptx::pack_bf16x2(acc[j + 1].x, acc[j + 1].y),
+                                            ptx::pack_bf16x2(acc[j + 1].z, acc[j + 1].w));
+        }
+        if (half == 0)
+          p.lse[((size_t)(seq / p.NQT) * p.H + gr % p.H) * p.T + gr / p.H] =
+              wsum > 0.f ? mxl + logf(wsum) : -INFINITY;
+      }
     }
   }
   ptx::tc_fence_before();
@@ -625,6 +735,13 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 512);
   }
+}
+
+// Zeroes the split counters of a decode call; the split kernel is launched behind it as a
+// programmatic dependent and waits for it only where it first touches a counter.
+__global__ void __launch_bounds__(256) zero_counters_kernel(int* __restrict__ c, int n) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  for (int i = threadIdx.x; i < n; i += blockDim.x) c[i] = 0;
 }
 
 }  // namespace sm103_decode
@@ -639,8 +756,8 @@ cudaError_t launch_decode_sm103(const void* q_latent, const void* q_rope, const 
                                 const float* kv_scale, const int* page_table,
                                 const int* cache_lens, int B, int H, int T, int max_pages,
                                 int num_pages, float softmax_scale, int causal, bool fp8,
-                                float* part_o, float* part_lse, int G, unsigned int* err,
-                                cudaStream_t stream) {
+                                float* part_o, float* part_lse, int* counters, void* out,
+                                float* lse, int G, unsigned int* err, cudaStream_t stream) {
   using namespace sm103_decode;
   CUtensorMap tm;
   // the cache as a 2-D tensor [num_pages * 64 rows, 576 columns]; boxes of 64 x 64
@@ -673,23 +790,52 @@ cudaError_t launch_decode_sm103(const void* q_latent, const void* q_rope, const 
   p.cache_lens = cache_lens;
   p.part_o = part_o;
   p.part_lse = part_lse;
+  p.counters = counters;
+  p.out = static_cast<uint16_t*>(out);
+  p.lse = lse;
   p.err = err;
   p.B = B;
   p.H = H;
   p.T = T;
   p.NQT = (TH + 127) / 128;
   p.TQ = TQ;
+  p.n_slots = G + B * p.NQT;
   p.max_pages = max_pages;
   p.num_pages = num_pages;
   p.causal = causal;
   p.G = G;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  // the split counters of the merge start at zero on every call
+  const long long n_cnt = 2LL * B * p.NQT;
+  if (n_cnt > 0x7fffffffLL) return cudaErrorInvalidValue;
+  // same shared-memory carveout as the split kernel, so the SMs are not reconfigured between
+  // the two launches
+  static int carveout_set = 0;
+  if (!__atomic_load_n(&carveout_set, __ATOMIC_ACQUIRE)) {
+    if ((e = cudaFuncSetAttribute(zero_counters_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+      return e;
+    __atomic_store_n(&carveout_set, 1, __ATOMIC_RELEASE);
+  }
+  zero_counters_kernel<<<1, 256, 0, stream>>>(counters, (int)n_cnt);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   auto go = [&](auto kern) -> cudaError_t {
     static unsigned long long smem_set[2] = {0, 0};
     const cudaError_t e2 = smem_attr_once(kern, kSmemAlloc, &smem_set[fp8 ? 1 : 0]);
     if (e2 != cudaSuccess) return e2;
-    kern<<<2 * G, fp8 ? kThreadsOf<true> : kThreadsOf<false>, kSmemAlloc, stream>>>(tm, tm_qlat, tm_qrope, p);
-    return cudaGetLastError();
+    // programmatic dependent of the zeroing kernel: the prologue (barriers, TMEM, plan, first
+    // loads) overlaps it
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * G);
+    cfg.blockDim = dim3(fp8 ? kThreadsOf<true> : kThreadsOf<false>);
+    cfg.dynamicSmemBytes = kSmemAlloc;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tm, tm_qlat, tm_qrope, p);
   };
   return fp8 ? go(decode_split_kernel<true>) : go(decode_split_kernel<false>);
 }

@@ -25,11 +25,8 @@ cudaError_t launch_decode_sm103(const void* q_latent, const void* q_rope, const 
                                 const float* kv_scale, const int* page_table,
                                 const int* cache_lens, int B, int H, int T, int max_pages,
                                 int num_pages, float softmax_scale, int causal, bool fp8,
-                                float* part_o, float* part_lse, int G, unsigned int* err,
-                                cudaStream_t stream);
-cudaError_t launch_decode_combine(const float* part_o, const float* part_lse,
-                                  const int* cache_lens, void* out, float* lse, int B, int H,
-                                  int T, int max_pages, int G, cudaStream_t stream);
+                                float* part_o, float* part_lse, int* counters, void* out,
+                                float* lse, int G, unsigned int* err, cudaStream_t stream);
 cudaError_t launch_absorb_sm103(const void* x, const void* w, void* y, int R, int H, int K, int N,
                                 unsigned int* err, cudaStream_t stream);
 size_t prefill_bwd_workspace_bytes(int B, int H, int S);
@@ -96,21 +93,25 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct DecodeWorkspace {
   float* part_o;
   float* part_lse;
+  int* counters;
   size_t bytes;
 };
 
 // The q_len*H query rows of a sequence are processed in tiles of (up to) 128 rows; each
 // (sequence, tile) is planned as its own work item, so there are G + B * NQT partial slots of
-// TQ = min(q_len*H, 128) rows each.
+// TQ = min(q_len*H, 128) rows each: O partials (fp32, 512 columns), LSE partials (one copy per
+// column half), and two split counters per work item for the merge.
 DecodeWorkspace decode_workspace_layout(void* base, int B, int TH, int d_latent, int G) {
   DecodeWorkspace w;
   const size_t nqt = (size_t)(TH + 127) / 128, tq = TH < 128 ? TH : 128;
   const size_t slots = (size_t)G + (size_t)B * nqt;
   const size_t o_bytes = align_up(slots * tq * d_latent * sizeof(float), 256);
-  const size_t l_bytes = align_up(slots * tq * sizeof(float), 256);
+  const size_t l_bytes = align_up(2 * slots * tq * sizeof(float), 256);
+  const size_t c_bytes = align_up(2 * (size_t)B * nqt * sizeof(int), 256);
   w.part_o = static_cast<float*>(base);
   w.part_lse = reinterpret_cast<float*>(static_cast<char*>(base) + o_bytes);
-  w.bytes = o_bytes + l_bytes;
+  w.counters = reinterpret_cast<int*>(static_cast<char*>(base) + o_bytes + l_bytes);
+  w.bytes = o_bytes + l_bytes + c_bytes;
   return w;
 }
 
@@ -292,10 +293,7 @@ mla_status mla_decode(const void* q_latent, const void* q_rope, const void* kv_c
   cudaError_t e = mla::launch_decode_sm103(q_latent, q_rope, kv_cache, kv_scale, page_table,
                                            cache_lens, B, H, q_len, max_pages_per_seq, num_pages,
                                            softmax_scale, causal != 0, fp8, ws.part_o,
-                                           ws.part_lse, G, err, st);
-  if (e == cudaSuccess)
-    e = mla::launch_decode_combine(ws.part_o, ws.part_lse, cache_lens, out, lse, B, H, q_len,
-                                   max_pages_per_seq, G, st);
+                                           ws.part_lse, ws.counters, out, lse, G, err, st);
   if (e != cudaSuccess) return cuda_fail(e, "mla_decode launch");
   return MLA_OK;
 }

@@ -1,4 +1,5 @@
-"""GPU parity of mla_decode (split-KV + combine, through the C ABI) against the fp64 oracle."""
+"""GPU parity of mla_decode (split-KV with the merge of the splits fused in, through the C ABI)
+against the fp64 oracle."""
 import numpy as np
 import pytest
 import torch
