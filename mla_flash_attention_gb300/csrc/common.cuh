@@ -32,12 +32,12 @@ __device__ __forceinline__ int pages_of(int L, int page_size) {
   return L > 0 ? (L + page_size - 1) / page_size : 0;
 }
 
-// Split plan of the decode key axis (computed identically by every kernel that needs
-// it, from cache_lens alone): the pages of all sequences are numbered in sequence
-// order (sequence b owns flat pages [P_b, P_b + n_b)), and work unit c of G takes flat
-// pages [c*chunk, (c+1)*chunk) with chunk = ceil(total / G).  The partial result of
-// unit c for sequence b goes to slot c + b, which is unique because consecutive units
-// never move backwards through the sequences; there are at most G + B - 1 slots.
+// Split plan of the decode key axis (computed from cache_lens alone, identically by every
+// CTA of the split kernel): the pages of all (sequence, query tile) work items are numbered
+// in order (item v owns flat pages [P_v, P_v + n_v)), and work unit c of G takes flat pages
+// [c*chunk, (c+1)*chunk) with chunk = ceil(total / G).  The partial result of unit c for
+// item v goes to slot c + v, which is unique because consecutive units never move backwards
+// through the items; there are at most G + (number of items) - 1 slots.
 
 // Opt `kernel` into `bytes` of dynamic shared memory on the current device.  The attribute
 // belongs to the device, so it is set once per device ordinal: `done` holds one bit per

@@ -1,4 +1,5 @@
-// Absorbed MLA decode over the paged latent cache on tcgen05 / TMEM (split-KV part).
+// Absorbed MLA decode over the paged latent cache on tcgen05 / TMEM: split-KV, with the
+// log-sum-exp merge of the splits done by the last split of each sequence to finish.
 //
 // Each work unit (a contiguous range of pages from the split plan) is served by a pair
 // of CTAs that differ only in which half of the 512 latent output columns they own:
@@ -22,7 +23,9 @@
 //   (+ 8-11)    fp8: widen the page to bf16 in place (three chunks of one row per thread;
 //               warps 8-11 exist in the fp8 kernel only) and stage its scales
 //   warps 4-7   softmax, one thread per query row; they also write the split's partial
-//               (O_half / l, log-sum-exp), column quads of 32 rows per 512-byte store
+//               (O_half / l, log-sum-exp), column quads of 32 rows per 512-byte store, and,
+//               in the CTA that completes a (sequence, column half), merge its splits into
+//               the bf16 output and the LSE
 // TMEM columns: [0,128) Q latent 0..255 (bf16 pairs), [128,256) two S / P buffers of 64,
 // [256,512) O half.
 #include <cuda.h>
