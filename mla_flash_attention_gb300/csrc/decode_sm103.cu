@@ -31,6 +31,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "sm103_ptx.cuh"
 
@@ -744,7 +746,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
 // programmatic dependent and waits for it only where it first touches a counter.
 __global__ void __launch_bounds__(256) zero_counters_kernel(int* __restrict__ c, int n) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  for (int i = threadIdx.x; i < n; i += blockDim.x) c[i] = 0;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) c[i] = 0;
 }
 
 }  // namespace sm103_decode
@@ -820,7 +822,8 @@ cudaError_t launch_decode_sm103(const void* q_latent, const void* q_rope, const 
       return e;
     __atomic_store_n(&carveout_set, 1, __ATOMIC_RELEASE);
   }
-  zero_counters_kernel<<<1, 256, 0, stream>>>(counters, (int)n_cnt);
+  const int zero_blocks = (int)std::min<long long>((n_cnt + 2047) / 2048, 1024);
+  zero_counters_kernel<<<zero_blocks, 256, 0, stream>>>(counters, (int)n_cnt);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   auto go = [&](auto kern) -> cudaError_t {
     static unsigned long long smem_set[2] = {0, 0};
