@@ -56,7 +56,9 @@ struct Params {
 };
 
 struct Bars {
-  uint64_t fix_full, ring_full[2], ring_empty[2], one_full, one_empty;
+  // one full barrier per 16 KB chunk of a streamed tile, so the MMAs over its first chunk can
+  // start while the later ones are still arriving
+  uint64_t fix_full, ring_full[2][3], ring_empty[2], one_full[2], one_empty;
   uint64_t s_full, x_read, dp_full, dp_read, p_ready, dv_done, ds_ready, acc_step, acc_done;
   uint32_t tmem_base;
   int abort_flag;
@@ -207,26 +209,29 @@ __device__ __forceinline__ void bwd_body(const Maps& m, const Params& p, unsigne
         if (!ptx::mbar_wait(&bars.ring_empty[s], ((n >> 1) & 1) ^ 1, abort_flag, p.err)) break;
         unsigned char* dst = sm + kOffRing + s * 3 * kChunk;
         if (kKeyRole) {
-          ptx::mbar_arrive_expect_tx(&bars.ring_full[s], 3 * kChunk + 2 * BT * 4);
-          ptx::tma_load_4d(dst, m.qn, &bars.ring_full[s], 0, h, r0, b);
-          ptx::tma_load_4d(dst + kChunk, m.qn, &bars.ring_full[s], 64, h, r0, b);
-          ptx::tma_load_4d(dst + 2 * kChunk, m.qr, &bars.ring_full[s], 0, h, r0, b);
+          ptx::mbar_arrive_expect_tx(&bars.ring_full[s][0], kChunk + 2 * BT * 4);
+          ptx::mbar_arrive_expect_tx(&bars.ring_full[s][1], kChunk);
+          ptx::mbar_arrive_expect_tx(&bars.ring_full[s][2], kChunk);
+          ptx::tma_load_4d(dst, m.qn, &bars.ring_full[s][0], 0, h, r0, b);
+          ptx::tma_load_4d(dst + kChunk, m.qn, &bars.ring_full[s][1], 64, h, r0, b);
+          ptx::tma_load_4d(dst + 2 * kChunk, m.qr, &bars.ring_full[s][2], 0, h, r0, b);
           const size_t vo = (size_t)bh * p.S_pad + r0;
           unsigned char* vec = sm + kOffVec + s * 2 * BT * 4;
-          ptx::bulk_load(vec, p.nlse2 + vo, BT * 4, &bars.ring_full[s]);
-          ptx::bulk_load(vec + BT * 4, p.dvec + vo, BT * 4, &bars.ring_full[s]);
+          ptx::bulk_load(vec, p.nlse2 + vo, BT * 4, &bars.ring_full[s][0]);
+          ptx::bulk_load(vec + BT * 4, p.dvec + vo, BT * 4, &bars.ring_full[s][0]);
         } else {
-          ptx::mbar_arrive_expect_tx(&bars.ring_full[s], 3 * kChunk);
-          ptx::tma_load_4d(dst, m.kn, &bars.ring_full[s], 0, h, r0, b);
-          ptx::tma_load_4d(dst + kChunk, m.kn, &bars.ring_full[s], 64, h, r0, b);
-          ptx::tma_load_3d(dst + 2 * kChunk, m.kr, &bars.ring_full[s], 0, r0, b);
+          for (int c = 0; c < 3; ++c) ptx::mbar_arrive_expect_tx(&bars.ring_full[s][c], kChunk);
+          ptx::tma_load_4d(dst, m.kn, &bars.ring_full[s][0], 0, h, r0, b);
+          ptx::tma_load_4d(dst + kChunk, m.kn, &bars.ring_full[s][1], 64, h, r0, b);
+          ptx::tma_load_3d(dst + 2 * kChunk, m.kr, &bars.ring_full[s][2], 0, r0, b);
         }
         if (!ptx::mbar_wait(&bars.one_empty, (n & 1) ^ 1, abort_flag, p.err)) break;
         unsigned char* one = sm + kOffOne;
         const CUtensorMap* tm = kKeyRole ? m.dout : m.v;
-        ptx::mbar_arrive_expect_tx(&bars.one_full, 2 * kChunk);
-        ptx::tma_load_4d(one, tm, &bars.one_full, 0, h, r0, b);
-        ptx::tma_load_4d(one + kChunk, tm, &bars.one_full, 64, h, r0, b);
+        ptx::mbar_arrive_expect_tx(&bars.one_full[0], kChunk);
+        ptx::mbar_arrive_expect_tx(&bars.one_full[1], kChunk);
+        ptx::tma_load_4d(one, tm, &bars.one_full[0], 0, h, r0, b);
+        ptx::tma_load_4d(one + kChunk, tm, &bars.one_full[1], 64, h, r0, b);
       }
     }
     __syncwarp();
@@ -241,11 +246,13 @@ __device__ __forceinline__ void bwd_body(const Maps& m, const Params& p, unsigne
       auto ring_of = [&](int n) { return base + kOffRing + (n & 1) * 3 * kChunk; };
       // scores over the 192-deep nope+rope contraction (key role: transposed, keys on lanes)
       auto issue_s = [&](int n) -> bool {
-        if (!ptx::mbar_wait(&bars.ring_full[n & 1], (n >> 1) & 1, abort_flag, p.err)) return false;
-        ptx::tc_fence_after();
         const uint32_t ring = ring_of(n);
 #pragma unroll
         for (int k = 0; k < 12; ++k) {
+          if ((k & 3) == 0) {  // each 64-deep chunk as soon as it has landed
+            if (!ptx::mbar_wait(&bars.ring_full[n & 1][k >> 2], (n >> 1) & 1, abort_flag, p.err)) return false;
+            ptx::tc_fence_after();
+          }
           const uint32_t off = (k >> 2) * kChunk + (k & 3) * 32;
           ptx::mma_bf16_ss(tmem + kColX, ptx::sw128_desc(base + kOffFix3 + off, 16, 1024),
                            ptx::sw128_desc(ring + off, 16, 1024), kIdS, k > 0);
@@ -255,10 +262,12 @@ __device__ __forceinline__ void bwd_body(const Maps& m, const Params& p, unsigne
       };
       // dP = dO V' over d_v = 128 (key role: dP' = V dO' into X; query role: own columns)
       auto issue_dp = [&](int n) -> bool {
-        if (!ptx::mbar_wait(&bars.one_full, n & 1, abort_flag, p.err)) return false;
-        ptx::tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
+          if ((k & 3) == 0) {
+            if (!ptx::mbar_wait(&bars.one_full[k >> 2], n & 1, abort_flag, p.err)) return false;
+            ptx::tc_fence_after();
+          }
           const uint32_t off = (k >> 2) * kChunk + (k & 3) * 32;
           ptx::mma_bf16_ss(tmem + (kKeyRole ? kColX : kColDP),
                            ptx::sw128_desc(base + kOffFix2 + off, 16, 1024),
@@ -351,7 +360,7 @@ __device__ __forceinline__ void bwd_body(const Maps& m, const Params& p, unsigne
       const float* vec = reinterpret_cast<const float*>(sm + kOffVec + s * 2 * BT * 4);
       ok = wait(&bars.s_full, n & 1);
       // the query vectors of this stage arrived with its TMA transaction: observe it directly
-      if (kKeyRole && ok) ok = wait(&bars.ring_full[s], (n >> 1) & 1);
+      if (kKeyRole && ok) ok = wait(&bars.ring_full[s][0], (n >> 1) & 1);
       if (!ok) break;
       uint32_t u[64];
       ptx::tmem_ld32(tX, *reinterpret_cast<uint32_t(*)[32]>(u));
@@ -517,10 +526,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     bars.abort_flag = 0;
     ptx::mbar_init(&bars.fix_full, 1);
     for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(&bars.ring_full[s], 1);
+      for (int c = 0; c < 3; ++c) ptx::mbar_init(&bars.ring_full[s][c], 1);
       ptx::mbar_init(&bars.ring_empty[s], 1);
     }
-    ptx::mbar_init(&bars.one_full, 1);
+    ptx::mbar_init(&bars.one_full[0], 1);
+    ptx::mbar_init(&bars.one_full[1], 1);
     ptx::mbar_init(&bars.one_empty, 1);
     ptx::mbar_init(&bars.s_full, 1);
     ptx::mbar_init(&bars.x_read, 8);    // one arrival per elementwise warp
