@@ -99,8 +99,10 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restric
       part[r] = fmaf(hi(a.y), hi(o.y), acc);
     }
   }
-  // after the round with offset w, part[0 .. w) of lane l hold partial sums of rows
-  // (l & ~(2w-1) & 31) ... ; at the end part[0] of lane l is the full sum of row l
+  // Each exchange with offset w halves the rows a lane keeps: lanes with bit w set keep the
+  // upper half of their remaining rows, the others the lower half, and each adds its
+  // partner's partial sums of the rows it keeps.  After w = 16, 8, 4, 2, 1, part[0] of lane
+  // l holds row l summed over all 32 lanes.
 #pragma unroll
   for (int w = 16; w >= 1; w >>= 1) {
     const bool upper = (lane & w) != 0;

@@ -16,7 +16,7 @@ What is computed (the pages' vocabulary):
 * Per-token fp32 ``q_scale`` / ``k_scale`` (same page, Fields ``q_scale_smem``,
   ``k_scale_smem``: one float per query row of a tile and per key row).
 
-Readings where the pages are silent (each is also listed in the design doc):
+Readings where the pages are silent (the oracle pin tests exercise each one):
 
 * softmax_scale multiplies the whole nope+rope dot product; LSE is the natural
   log-sum-exp of the scaled scores (natural log, ``[B,H,S]`` / ``[B,H,T]``).
