@@ -123,3 +123,39 @@ def test_backward_argument_checks(clib):
     assert _backward(clib, scale=-1.0) == 1
     assert _backward(clib) == 3                  # no workspace
     assert _backward(clib, ws=16, wsb=100) == 3  # workspace too small
+
+
+def test_absorb_argument_checks(clib):
+    f = clib.mla_absorb
+    f.restype = ctypes.c_int
+    P = ctypes.c_void_p
+
+    def call(x=16, w=16, y=16, R=4, H=2, K=64, N=128):
+        return f(P(x), P(w), P(y), R, H, K, N, None)
+
+    assert call(x=None) == 1
+    assert call(R=0) == 1
+    assert call(K=96) == 2           # K must be a multiple of 64
+    assert call(N=64) == 2           # N must be a multiple of 128
+    assert call(y=24) == 1           # misaligned
+    assert call(H=70000) == 2
+
+
+def test_cache_append_argument_checks(clib):
+    f = clib.mla_cache_append
+    f.restype = ctypes.c_int
+    P = ctypes.c_void_p
+
+    def call(c=16, cache=16, scale=None, pt=16, lens=16, B=1, T=1, dl=512, dr=64, ps=64, mp=1,
+             npages=1, dt=0):
+        return f(P(c), P(cache), P(scale), P(pt), P(lens), B, T, dl, dr, ps, mp, npages, dt, None)
+
+    assert call(c=None) == 1
+    assert call(B=0) == 1
+    assert call(dl=256) == 2
+    assert call(ps=32) == 2
+    assert call(dt=1) == 1           # fp8 cache without scales
+    assert call(scale=16) == 1       # bf16 cache with scales
+    assert call(dt=1, scale=18) == 1  # scales not 4-byte aligned
+    assert call(cache=40) == 1       # misaligned
+    assert call(dt=5) == 2
