@@ -216,7 +216,12 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   __shared__ Bars bars;
-  constexpr int kThreads = kThreadsOf<kFp8>, kPrepThreads = kPrepOf<kFp8>;
+  constexpr int kThreads = kThreadsOf<kFp8>;
+  // fp8: with fewer than 128 query rows per tile, softmax warps whose 32 rows are all padding
+  // of the M = 128 MMA (never stored) widen pages instead: warps 4 .. 4 + n_soft - 1 run the
+  // softmax, warps 4 + n_soft .. 7 join the preparation warps (2-3 and 8-11)
+  const int n_soft = kFp8 ? (p.TQ + 31) / 32 : kRows / 32;
+  const int n_prep = kPrepOf<kFp8> + (kFp8 ? 32 * (kRows / 32 - n_soft) : 0);
   constexpr int kParts = kFp8 ? 3 : 1;  // readiness parts of a page stage
   const int warp = threadIdx.x >> 5;
   const int unit = blockIdx.x >> 1, half = blockIdx.x & 1;
@@ -228,12 +233,12 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
     bars.abort_flag = 0;
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&bars.stage_full[s], 1);
-      for (int k = 0; k < 3; ++k) ptx::mbar_init(&bars.stage_ready[s][k], kPrepThreads / 32);
+      for (int k = 0; k < 3; ++k) ptx::mbar_init(&bars.stage_ready[s][k], n_prep / 32);
       ptx::mbar_init(&bars.stage_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&bars.s_full[i], 1);
-      ptx::mbar_init(&bars.p_full[i], kRows / 32);  // one arrival per softmax warp
+      ptx::mbar_init(&bars.p_full[i], n_soft);  // one arrival per softmax warp
     }
     ptx::mbar_init(&bars.o_done, 1);
     ptx::mbar_init(&bars.seg_done, 1);
@@ -241,8 +246,8 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
     ptx::mbar_init(&bars.q_lo_full, 1);
     ptx::mbar_init(&bars.q_cp_done, 1);
     ptx::mbar_init(&bars.q_hi_full, 1);
-    ptx::mbar_init(&bars.conv_sync, kPrepThreads / 32);  // one arrival per preparation warp
-    ptx::mbar_init(&bars.part_done, kRows / 32);
+    ptx::mbar_init(&bars.conv_sync, n_prep / 32);  // one arrival per preparation warp
+    ptx::mbar_init(&bars.part_done, n_soft);
     ptx::mbar_init(&bars.merge_go, 1);
     ptx::fence_barrier_init();
   }
@@ -414,9 +419,12 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
         ++nseg;
       }
     }
-  } else if (warp < 4 || warp >= 8) {
+  } else if (warp < 4 || warp >= 8 || warp >= 4 + n_soft) {
     // -------------------------------------------------------------- stage preparation
-    const int tid = warp < 4 ? threadIdx.x - 64 : threadIdx.x - 192;  // 0 .. kPrepThreads-1
+    // 0 .. n_prep - 1: warps 2-3, then 8-11, then the softmax warps that joined
+    const int tid = warp < 4 ? threadIdx.x - 64
+                  : warp >= 8 ? threadIdx.x - 192
+                              : kPrepOf<kFp8> + threadIdx.x - 32 * (4 + n_soft);
     const int row = tid & (kPage - 1);  // the page row whose scale (fp8) this thread stages
     int g = 0;
     bool ok = true;
@@ -438,7 +446,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
           if (valid < kPage) {
             // zero rows valid..63 of all 9 chunks (16-byte granules)
             const int nrow = kPage - valid;
-            for (int e = tid; e < nrow * 9 * 8; e += kPrepThreads) {
+            for (int e = tid; e < nrow * 9 * 8; e += n_prep) {
               const int row = valid + e / 72, rem = e % 72, c = rem >> 3, gr = rem & 7;
               *reinterpret_cast<uint4*>(st + c * kPageChunk + row * 128 + gr * 16) = make_uint4(0, 0, 0, 0);
             }
@@ -457,12 +465,13 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
 #pragma unroll 1
           for (int k = 0; k < 3 && ok; ++k) {
             // the step's 3 chunks are 768 granules of 16 raw bytes (64 rows x 4 per chunk);
-            // thread tid takes granules tid + 192 q, so a warp reads 512 contiguous bytes
+            // thread tid takes granules tid + n_prep q (at most four: n_prep >= 192), so a warp
+            // reads 512 contiguous bytes
             uint4 raw[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const int G = tid + kPrepThreads * q, c = 3 * k + (G >> 8), gi = G & 255;
-              raw[q] = (live_row(gi >> 2))
+              const int G = tid + n_prep * q, c = 3 * k + (G >> 8), gi = G & 255;
+              raw[q] = (G < 768 && live_row(gi >> 2))
                            ? *reinterpret_cast<const uint4*>(st + kRawOffset + c * kRawChunk + gi * 16)
                            : make_uint4(0, 0, 0, 0);
             }
@@ -472,7 +481,8 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
             if (!ok) break;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const int G = tid + kPrepThreads * q, c = 3 * k + (G >> 8), gi = G & 255;
+              const int G = tid + n_prep * q, c = 3 * k + (G >> 8), gi = G & 255;
+              if (G >= 768) continue;
               const int rw = gi >> 2, quarter = gi & 3;  // 16 columns 16 quarter .. of row rw
               const uint32_t words[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
               uint32_t w[8];
@@ -506,8 +516,8 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
       for (int b = unit; b < p.B; b += p.G) {
         if (clamp_len(__ldg(p.cache_lens + b), p.max_pages) > 0) continue;
         uint4* o = reinterpret_cast<uint4*>(p.out + (size_t)b * TH * kDl);
-        for (int i = r; i < TH * (kDl / 8); i += kRows) o[i] = make_uint4(0, 0, 0, 0);
-        for (int i = r; i < TH; i += kRows) p.lse[((size_t)b * p.H + i % p.H) * p.T + i / p.H] = -INFINITY;
+        for (int i = r; i < TH * (kDl / 8); i += 32 * n_soft) o[i] = make_uint4(0, 0, 0, 0);
+        for (int i = r; i < TH; i += 32 * n_soft) p.lse[((size_t)b * p.H + i % p.H) * p.T + i / p.H] = -INFINITY;
       }
     }
     while (ok && segs.next(seq, L, lo, hi)) {
