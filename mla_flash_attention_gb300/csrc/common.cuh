@@ -14,15 +14,6 @@ enum : unsigned int {
   kErrBadPage = 2u,     // a page-table entry outside [0, num_pages)
 };
 
-__device__ __forceinline__ float bf16_to_f32(uint16_t bits) {
-  return __uint_as_float(static_cast<uint32_t>(bits) << 16);
-}
-
-__device__ __forceinline__ uint16_t f32_to_bf16_rne(float x) {
-  __nv_bfloat16 h = __float2bfloat16_rn(x);
-  return *reinterpret_cast<uint16_t*>(&h);
-}
-
 __device__ __forceinline__ void latch_error(unsigned int* err, unsigned int bits) {
   if (err) atomicOr(err, bits);
 }
