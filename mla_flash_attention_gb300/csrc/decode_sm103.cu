@@ -8,7 +8,7 @@
 // part) and their own half of O += P C[:, half].  Query rows are the (token, head) pairs
 // of one sequence, padded to the MMA's M = 128.
 //
-// Per CTA (8 warps):
+// Per CTA (8 warps; 12 with the fp8 cache):
 //   warp 0      TMA producer: each sequence's Q latent 0..255 (staged in shared memory),
 //               then one cache page (64 keys x 576 columns) per stage, as nine 64-column
 //               chunks -- bf16: 128B-swizzled, ready for the MMA; fp8: raw bytes into the
@@ -20,8 +20,10 @@
 //               with P read from TMEM.  S(g+1) and PV(g) are issued in whichever order their
 //               inputs arrive.
 //   warps 2-3   stage preparation: zero the rows past the sequence end of a partial page;
-//   (+ 8-11)    fp8: widen the page to bf16 in place (three chunks of one row per thread;
-//               warps 8-11 exist in the fp8 kernel only) and stage its scales
+//   (+ 8-11)    fp8: widen the page to bf16 in place (three lockstep steps of three
+//               64-column chunks, 16-byte granules spread over the preparation threads;
+//               warps 8-11 exist in the fp8 kernel only, and softmax warps whose 32 rows
+//               are all padding of the M = 128 MMA join them) and stage its scales
 //   warps 4-7   softmax, one thread per query row; they also write the split's partial
 //               (O_half / l, log-sum-exp), column quads of 32 rows per 512-byte store, and,
 //               in the CTA that completes a (sequence, column half), merge its splits into
