@@ -1,12 +1,14 @@
 """Randomised pins of the oracle (CPU): over drawn shapes, masks, scales and cache layouts the
 oracle equals torch's scaled_dot_product_attention in float64 on the same dequantised
-operands, and its LSE is that of torch.logsumexp over the visible scaled scores."""
+operands, its LSE is that of torch.logsumexp over the visible scaled scores, and its
+backward equals torch autograd through the same SDPA."""
 import numpy as np
 import pytest
 import torch
+import torch.nn.functional as F
 
 import oracle
-from gen import make_decode, make_prefill
+from gen import make_decode, make_grad_out, make_prefill
 from tests.test_oracle_pins import _decode_sdpa, sdpa, t_bf16, t_e4m3
 
 hyp = pytest.importorskip("hypothesis")
@@ -65,3 +67,25 @@ def test_decode_matches_sdpa_on_drawn_problems(lens, H, T, fp8, causal, extra, s
         seen = mask.any(-1).reshape(T, H).numpy()
         np.testing.assert_allclose(O[b][seen], ref.numpy()[seen], rtol=0, atol=1e-11)
         assert (O[b][~seen] == 0).all() and np.isneginf(L[b].T[~seen]).all()
+
+
+@hyp.settings(max_examples=20, deadline=None)
+@hyp.given(B=st.integers(1, 2), H=st.integers(1, 3), S=st.integers(1, 24),
+           dims=st.sampled_from([(16, 8, 12), (8, 4, 8)]), causal=st.booleans(),
+           scale=st.sampled_from([0.1, 0.37, 1.0]), seed=st.integers(0, 10**6))
+def test_backward_matches_autograd_on_drawn_problems(B, H, S, dims, causal, scale, seed):
+    dn, dr, dv = dims
+    inp = make_prefill(B, H, S, d_nope=dn, d_rope=dr, d_v=dv, seed=seed, causal=causal,
+                       softmax_scale=scale)
+    dO_bits = make_grad_out(B, S, H, dv, seed=seed + 1)
+    f = oracle.bf16_to_f64
+    leaves = {n: torch.tensor(f(getattr(inp, n)), requires_grad=True)
+              for n in ("q_nope", "q_rope", "k_nope", "k_rope", "v")}
+    q = torch.cat([leaves["q_nope"], leaves["q_rope"]], -1).transpose(1, 2)
+    k = torch.cat([leaves["k_nope"], leaves["k_rope"][:, :, None, :].expand(B, S, H, dr)], -1).transpose(1, 2)
+    o = F.scaled_dot_product_attention(q, k, leaves["v"].transpose(1, 2), is_causal=causal, scale=scale)
+    o.transpose(1, 2).backward(torch.tensor(f(dO_bits)))
+    got = dict(zip(("q_nope", "q_rope", "k_nope", "k_rope", "v"), oracle.mla_prefill_backward(inp, dO_bits)))
+    for name, t in leaves.items():
+        g = t.grad.numpy()
+        np.testing.assert_allclose(got[name], g, rtol=0, atol=1e-10 * max(1.0, np.abs(g).max()), err_msg=name)
