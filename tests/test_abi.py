@@ -72,6 +72,15 @@ def test_prefill_argument_checks(clib):
     assert b"softmax_scale" in clib.mla_last_error()
 
 
+def test_prefill_size_limits(clib):
+    # the largest sizes the kernels index are enforced on the host (MLA_ERR_UNSUPPORTED)
+    assert _prefill(clib, B=65536) == 2
+    assert _prefill(clib, H=65536) == 2
+    assert _prefill(clib, B=65535, H=65535, S=2**31 - 1) == 2   # B*S*H*128 beyond int64 indexing
+    clib.mla_last_error.restype = ctypes.c_char_p
+    assert b"too large" in clib.mla_last_error()
+
+
 def _decode(clib, **kw):
     a = dict(ql=16, qr=16, cache=16, ks=None, pt=16, lens=16, out=16, lse=16, B=1, H=16, T=1,
              dl=512, dr=64, ps=64, mp=1, npages=1, scale=0.1, causal=1, dt=0, ws=None, wsb=0)
@@ -95,6 +104,14 @@ def test_decode_argument_checks(clib):
     assert _decode(clib, ks=16) == 1           # bf16 with scales
     assert _decode(clib, out=8) == 1           # misaligned
     assert _decode(clib, npages=0) == 1
+
+
+def test_decode_size_limits(clib):
+    assert _decode(clib, B=65536, H=1) == 2                 # one work item per sequence: B <= 65535
+    assert _decode(clib, B=65535, H=128, T=512) == 2        # B * 512 query tiles > 2^24
+    assert _decode(clib, mp=2**26) == 2                     # max_pages * 64 overflows int32
+    clib.mla_last_error.restype = ctypes.c_char_p
+    assert b"overflows" in clib.mla_last_error()
 
 
 def _backward(clib, **kw):
