@@ -74,11 +74,6 @@ def library_path() -> str:
     return _LIB_PATH
 
 
-def raw():
-    """The ctypes library handle (for tests that exercise the C ABI directly)."""
-    return _lib
-
-
 def _check(st: int):
     if st != MLA_OK:
         raise MLAError(st, _lib.mla_last_error().decode(errors="replace"))

@@ -4,7 +4,7 @@ import pytest
 import torch
 
 import oracle
-from gen import CONFIGS, config_inputs, make_prefill
+from gen import config_inputs, make_prefill
 from tests.parity import TOL_O_BF16, TOL_O_FP8, check
 
 pytestmark = pytest.mark.gpu

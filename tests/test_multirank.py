@@ -1,5 +1,4 @@
 """The N>1 bench path (independent replicas, max-over-ranks timing) on CPU with gloo ranks."""
-import os
 import socket
 
 import pytest
