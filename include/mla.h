@@ -76,7 +76,8 @@ typedef enum {
  *   lse     [B, H, S] fp32
  * causal != 0: query i sees keys 0..i (square problem).  causal == 0: all keys.
  * Supported: d_nope = 128, d_rope = 64, d_v = 128; qkv_dtype MLA_BF16 or
- * MLA_FP8_E4M3; S >= 1; B*H*S*max(d) < 2^31 per tensor dimension product.
+ * MLA_FP8_E4M3; S >= 1; B, H <= 65535 (offsets are 64-bit; B*S*H*128 must stay below
+ * 9e18).  Larger sizes return MLA_ERR_UNSUPPORTED.
  */
 mla_status mla_prefill(const void* q_nope, const void* q_rope, const void* k_nope,
                        const void* k_rope, const void* v, const float* q_scale,
@@ -112,7 +113,9 @@ size_t mla_decode_workspace_size(int B, int H, int q_len, int d_latent);
  * outside are reported through MLA_ERR_DEVICE_CHECK (that page is skipped).
  * Supported: d_latent = 512, d_rope = 64, page_size = 64, q_len * H <= 65536 (rows beyond
  * 128 are processed in tiles of 128 rows: q_len > 1 new tokens over a cached prefix is
- * chunked prefill in absorbed form, after mla_cache_append has written the chunk's rows).
+ * chunked prefill in absorbed form, after mla_cache_append has written the chunk's rows),
+ * B <= 65535, B * ceil(q_len * H / 128) <= 2^24, max_pages_per_seq * page_size < 2^31.
+ * Larger sizes return MLA_ERR_UNSUPPORTED.
  */
 mla_status mla_decode(const void* q_latent, const void* q_rope, const void* kv_cache,
                       const float* kv_scale, const int* page_table, const int* cache_lens,
@@ -207,7 +210,8 @@ size_t mla_prefill_backward_workspace_size(int B, int H, int S);
  *   dk_rope [B, S, d_rope] fp32 -- written in full (zeroed, then accumulated over heads)
  *   workspace  device buffer of at least mla_prefill_backward_workspace_size() bytes
  * causal as for mla_prefill.  All gradients are accumulated in fp32; P and dS enter the
- * products as bf16.  Supported: d_nope = 128, d_rope = 64, d_v = 128, bf16 only.
+ * products as bf16.  Supported: d_nope = 128, d_rope = 64, d_v = 128, bf16 only,
+ * B, H <= 65535 (larger: MLA_ERR_UNSUPPORTED).
  */
 mla_status mla_prefill_backward(const void* q_nope, const void* q_rope, const void* k_nope,
                                 const void* k_rope, const void* v, const void* out,
