@@ -132,16 +132,24 @@ mla_status mla_decode(const void* q_latent, const void* q_rope, const void* kv_c
  * therefore cannot supply mla_decode's workspace.)
  *
  * Arguments, layouts and results are those of mla_decode without the workspace: the split
- * partials go to a scratch array compiled into the library, of
- * mla_decode_noalloc_max_workspace() bytes (48 MiB), which every GPU that loads the library
- * holds until the process exits.  Allocates nothing.
+ * partials and merge counters go to a scratch array compiled into the library, of
+ * mla_decode_noalloc_max_workspace() bytes (48 MiB).  No call allocates or frees device memory
+ * through this library or the CUDA runtime's allocator.
+ *   - Set-up: the array lives in its own module.  Under CUDA's lazy module loading (the
+ *     default) the driver loads that module, and reserves the 48 MiB on the device, the first
+ *     time the array's address is looked up on that device; it is then held until the
+ *     process exits.  A call with B = 0 does only that set-up on the current device (looks up
+ *     the array's address with cudaGetSymbolAddress, loads the decode kernels and the device
+ *     error word), ignores every other argument and launches nothing.  A caller that reserves
+ *     device memory at start-up makes this call first, before its reservation and before any
+ *     stream capture; without it, the first ordinary call on the device does the set-up.
  *   - A batch whose mla_decode_workspace_size() exceeds that size is rejected with
  *     MLA_ERR_WORKSPACE before anything is launched.
- *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress);
- *     make that first call before any stream capture.
- *   - All calls on a device share the array, which keeps the last call's contents (nothing
- *     needs clearing: a call only reads what it wrote).  Calls that overlap on the GPU race
- *     on the array; the caller must serialise them (one stream, or ordered streams).
+ *   - All calls on a device share the array, which keeps the last call's contents.  Every
+ *     call writes its partials before reading them and zeroes the merge counters (with a
+ *     kernel queued ahead of the decode kernel) before counting, so nothing has to be cleared
+ *     by the caller.  Calls that overlap on the GPU race on the array; the caller must
+ *     serialise them (one stream, or ordered streams).
  */
 mla_status mla_decode_noalloc(const void* q_latent, const void* q_rope, const void* kv_cache,
                               const float* kv_scale, const int* page_table, const int* cache_lens,

@@ -285,6 +285,15 @@ def decode_noalloc_max_workspace() -> int:
     return int(_lib.mla_decode_noalloc_max_workspace())
 
 
+def mla_decode_noalloc_setup() -> None:
+    """The set-up call of mla_decode_noalloc on the current device (B = 0): the built-in
+    scratch array is reserved and the decode kernels are loaded, so that later calls on this
+    device allocate nothing.  Make it before reserving device memory and before any stream
+    capture."""
+    _check(_lib.mla_decode_noalloc(None, None, None, None, None, None, None, None, 0, 0, 0, 0, 0,
+                                   0, 0, 0, 0.0, 1, MLA_BF16, None))
+
+
 def mla_decode_noalloc(q_latent, q_rope, kv_cache, page_table, cache_lens, kv_scale=None, *,
                        softmax_scale: float, causal: bool = True, out=None, lse=None, stream=None):
     """mla_decode without a workspace: for callers that cannot allocate device memory at

@@ -765,6 +765,17 @@ __global__ void __launch_bounds__(256) zero_counters_kernel(int* __restrict__ c,
 
 // ---------------------------------------------------------------- host side
 
+// Makes the driver load every decode kernel on the current device (under lazy module loading
+// a kernel's module is otherwise loaded, and its device memory allocated, at its first launch).
+cudaError_t load_decode_kernels() {
+  using namespace sm103_decode;
+  cudaFuncAttributes fa;
+  cudaError_t e;
+  if ((e = cudaFuncGetAttributes(&fa, decode_split_kernel<false>)) != cudaSuccess) return e;
+  if ((e = cudaFuncGetAttributes(&fa, decode_split_kernel<true>)) != cudaSuccess) return e;
+  return cudaFuncGetAttributes(&fa, zero_counters_kernel);
+}
+
 cudaError_t encode_tensor_map_swz(CUtensorMap* map, CUtensorMapDataType dt, int rank,
                                   const void* ptr, const uint64_t* dims, const uint64_t* strides,
                                   const uint32_t* box, bool swizzle128);

@@ -2,6 +2,7 @@
 // device error word, decode workspace sizing and kernel dispatch.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -64,17 +65,21 @@ mla_status cuda_fail(cudaError_t e, const char* what) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Address of the device error word on the current device (looked up once per device).
+// Address of the device error word on the current device (looked up once per device).  The
+// cache entries are atomics: host threads may make their first calls concurrently, and two
+// threads that both look the address up store the same value.
 unsigned int* device_error_word() {
-  static unsigned int* cache[64] = {nullptr};
+  static std::atomic<unsigned int*> cache[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (!cache[dev]) {
+  unsigned int* w = cache[dev].load(std::memory_order_acquire);
+  if (!w) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
-    cache[dev] = static_cast<unsigned int*>(p);
+    w = static_cast<unsigned int*>(p);
+    cache[dev].store(w, std::memory_order_release);
   }
-  return cache[dev];
+  return w;
 }
 
 int num_sms_current() {
@@ -118,6 +123,9 @@ DecodeWorkspace decode_workspace_layout(void* base, int B, int TH, int d_latent,
 }  // namespace
 
 namespace mla {
+// The device error word's address on the current device (for entry points in other files).
+unsigned int* error_word_address() { return device_error_word(); }
+
 // Records `fmt` as this thread's last-error message (for entry points in other files).
 mla_status set_last_error(mla_status st, const char* fmt, ...) {
   char buf[512];

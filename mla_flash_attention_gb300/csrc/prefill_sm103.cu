@@ -35,6 +35,12 @@ constexpr int kOffRope = kOffRing + kRingSlots * 2 * kChunk;
 constexpr int kSmemBytes = kOffRope + kRopeSlots * kChunk;  // 224 KB
 constexpr int kSmemAlloc = kSmemBytes + 1024;
 constexpr int kThreads = 384;
+// registers per thread after the run-time hand-off (setmaxnreg): 128 producer/MMA threads
+// drop to kRegsLow, 256 softmax threads rise to kRegsHigh; the launch must provide their
+// average (rounded up to the allocation granule of 8)
+constexpr int kRegsLow = 56, kRegsHigh = 224;
+constexpr int kRegsAtLaunch = ((128 * kRegsLow + 256 * kRegsHigh + kThreads - 1) / kThreads + 7) / 8 * 8;
+static_assert(kRegsAtLaunch * kThreads <= 65536, "register hand-off exceeds the SM's file");
 
 struct Params {
   int B, H, S, causal, nrb, out_f32;
@@ -107,7 +113,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = &bars.abort_flag;
 
   if (warp < 4) {
-    ptx::regs_dec<56>();
+    ptx::regs_dec<kRegsLow>();
     if (warp == 0 && ptx::elect_one()) {
       // ------------------------------------------------------------ producer
       ptx::prefetch_tensormap(&tm_qn);
@@ -232,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // -------------------------------------------------------------- softmax warpgroups
-    ptx::regs_inc<224>();
+    ptx::regs_inc<kRegsHigh>();
     const int t = (warp >> 2) - 1;      // Q tile of this warpgroup
     const int r = (warp & 3) * 32 + lane;  // row within the tile == TMEM lane
     const int i = q_row0 + t * BM + r;     // query index
@@ -420,14 +426,16 @@ cudaError_t launch_prefill_sm103_bf16(const void* q_nope, const void* q_rope, co
   p.out = out;
   p.lse = lse;
   p.err = err;
-  // The warpgroups trade registers at run time (setmaxnreg): 128 threads drop to 56 and 256
-  // rise to 224, which needs exactly 168 per thread at launch.  Refuse otherwise.
+  // The warpgroups trade registers at run time (setmaxnreg): the producer/MMA warpgroup drops
+  // to kRegsLow and the two softmax warpgroups rise to kRegsHigh.  The raised counts are drawn
+  // from the registers the CTA was launched with, so the launch must give every thread at
+  // least their average; with fewer the raise would wait forever.  Refuse to launch then.
   static int regs_ok = 0;  // 0 unknown, 1 checked
   if (!__atomic_load_n(&regs_ok, __ATOMIC_ACQUIRE)) {
     cudaFuncAttributes fa;
     cudaError_t e = cudaFuncGetAttributes(&fa, prefill_bf16_kernel);
     if (e != cudaSuccess) return e;
-    if (fa.numRegs != 168) return cudaErrorInvalidDeviceFunction;
+    if (fa.numRegs < kRegsAtLaunch) return cudaErrorInvalidDeviceFunction;
     __atomic_store_n(&regs_ok, 1, __ATOMIC_RELEASE);
   }
   static unsigned long long smem_set = 0;

@@ -337,30 +337,6 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// 2^x on the FMA/ALU pipes, to take part of the exponentials off the special-function unit.
-// Cody-Waite style reduction x = n + f with n = round-to-nearest(x) (the 1.5 * 2^23 shift
-// leaves n in the low bits of t) and f in [-1/2, 1/2]; 2^f from a cubic fitted here to
-// minimise the relative error on that interval (Lawson's iteratively reweighted least
-// squares); 2^n is added to the exponent field.  Relative error <= 1.5e-4 over [-125, 8]
-// (well under the 2^-9 rounding of the bf16 probabilities it feeds).  x is clamped at
-// -125 (so the exponent field of 2^f * 2^n stays >= 1): masked scores (-inf) give
-// 2^-125 ~ 2.4e-38 instead of exactly 0.
-constexpr float kEx2C0 = 0.9999281167984009f;
-constexpr float kEx2C1 = 0.6932610273361206f;
-constexpr float kEx2C2 = 0.2426108419895172f;
-constexpr float kEx2C3 = 0.05517131835222244f;
-
-__device__ __forceinline__ float ex2_poly(float x) {
-  x = fmaxf(x, -125.f);
-  const float t = x + 12582912.0f;  // 1.5 * 2^23
-  const float n = t - 12582912.0f;
-  const float f = x - n;
-  float p = fmaf(f, kEx2C3, kEx2C2);
-  p = fmaf(p, f, kEx2C1);
-  p = fmaf(p, f, kEx2C0);
-  return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
-}
-
 // Two floats -> packed bf16x2 (round to nearest even); `lo` goes to the low half.
 // Packed single precision (two fp32 lanes in one 64-bit register pair; sm_100 and later):
 // one instruction performs both lanes' operation, each correctly rounded as its scalar form.

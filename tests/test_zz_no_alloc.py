@@ -4,7 +4,8 @@ It exists for callers that cannot allocate device memory where they run decode (
 that owns all device memory from start-up, a plugin hook that may not allocate), so they
 cannot hand mla_decode a workspace.  It must give the same results as mla_decode, call
 after call, even though every call reuses (and leaves behind) the same built-in scratch
-array.  This file is collected last so that a failure here cannot hide another test.
+array, and after its set-up call (B = 0) it must not change the device's free memory.
+This file is collected last so that a failure here cannot hide another test.
 """
 import numpy as np
 import pytest
@@ -57,3 +58,23 @@ def test_rejects_a_batch_larger_than_the_scratch(lib):
     d = _inputs(testing, inp)
     with pytest.raises(MLAError, match="WORKSPACE"):
         lib.mla_decode_noalloc(*d["args"], **d["kwargs"], softmax_scale=inp.softmax_scale)
+
+
+def test_allocates_nothing_after_the_setup_call(lib):
+    from mla_flash_attention_gb300 import testing
+
+    inp = make_decode(3, 16, 2, [900, 1, 4000], fp8=True, seed=54)
+    d = _inputs(testing, inp)
+    out = torch.empty((inp.B, inp.T, inp.H, inp.d_latent), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((inp.B, inp.H, inp.T), dtype=torch.float32, device="cuda")
+    lib.mla_decode_noalloc_setup()
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(2):
+        lib.mla_decode_noalloc(*d["args"], **d["kwargs"], softmax_scale=inp.softmax_scale,
+                               out=out, lse=lse)
+        torch.cuda.synchronize()
+        assert torch.cuda.mem_get_info()[0] == free0
+    lib.check_device_error()
+    O, L = oracle.mla_decode(inp)
+    check(out.float().cpu().numpy(), O, lse.cpu().numpy(), L, TOL_O_FP8, what="noalloc after set-up")
