@@ -56,12 +56,14 @@ _lib.mla_last_error.restype = ctypes.c_char_p
 _lib.mla_last_error.argtypes = []
 _lib.mla_version.restype = _i
 _lib.mla_version.argtypes = []
+_lib.mla_testing_decode_stall.restype = None
+_lib.mla_testing_decode_stall.argtypes = [_i, ctypes.c_longlong]
 
 EXPORTED = ("mla_prefill", "mla_decode_workspace_size", "mla_decode", "mla_decode_noalloc",
             "mla_decode_noalloc_max_workspace", "mla_cache_append", "mla_absorb",
             "mla_prefill_backward_workspace_size", "mla_prefill_backward",
             "mla_check_device_error",
-            "mla_last_error", "mla_version")
+            "mla_last_error", "mla_version", "mla_testing_decode_stall")
 
 
 class MLAError(RuntimeError):
@@ -103,6 +105,13 @@ def _need(t, name, dtype, shape):
 
 def version() -> int:
     return _lib.mla_version()
+
+
+def testing_decode_stall(skip_unit: int = -1, wait_limit_cycles: int = 0) -> None:
+    """Test hook (include/mla_testing.h): later fp8 decode calls with q_len*H <= 32 leave
+    pipeline unit `skip_unit` unloaded and give each device wait `wait_limit_cycles` SM clocks.
+    ``testing_decode_stall()`` restores normal calls."""
+    _lib.mla_testing_decode_stall(int(skip_unit), int(wait_limit_cycles))
 
 
 def check_device_error(stream=None) -> None:

@@ -36,12 +36,18 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "decode_plan.cuh"
 #include "sm103_ptx.cuh"
 
 namespace mla {
 namespace sm103_decode {
 
-constexpr int kPage = 64, kDl = 512, kDc = 576, kRows = 128;
+using decode_plan::Plan;
+using decode_plan::Segments;
+using decode_plan::clamp_len;
+using decode_plan::make_plan;
+constexpr int kPage = decode_plan::kPage;
+constexpr int kDl = 512, kDc = 576, kRows = 128;
 constexpr int kPageChunk = kPage * 128;       // 64 rows x 64 bf16 (8 KB), 128B-swizzled
 constexpr int kStageBytes = 9 * kPageChunk;   // 72 KB
 constexpr int kRawChunk = kPage * 64;         // 64 rows x 64 fp8 bytes (4 KB), unswizzled
@@ -75,12 +81,6 @@ struct Params {
   float scale_log2;
 };
 
-// The work unit's page range [start, end) of the flat page numbering and the first
-// sequence that reaches into it (b0, whose pages start at flat page pb0).
-struct Plan {
-  int start, end, b0, pb0, chunk;
-};
-
 struct Bars {
   // stage_ready[s][k]: bf16 pages are ready at once (k = 0); fp8 pages in three parts, k = 0..2
   // covering 64-column chunks 3k..3k+2, as the in-place widening completes them
@@ -93,114 +93,6 @@ struct Bars {
   int abort_flag;
   Plan plan;
   float kscale[kStages][kPage];
-};
-
-__device__ __forceinline__ int clamp_len(int L, int max_pages) {
-  return min(max(L, 0), max_pages * kPage);
-}
-
-__device__ __forceinline__ int warp_sum(int v) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  return v;
-}
-
-// The Plan of work unit `unit`, computed by one warp with coalesced loads of the lengths
-// (256 at a time) and warp scans.
-__device__ void make_plan(const Params& prm, int unit, Plan* out) {
-  const int lane = threadIdx.x & 31;
-  const int B = prm.B * prm.NQT;  // work is planned per (sequence, query tile)
-  auto pages_at = [&](int bb) {
-    return bb < B ? pages_of(clamp_len(__ldg(prm.cache_lens + bb / prm.NQT), prm.max_pages), kPage) : 0;
-  };
-  int total = 0;
-  for (int base = 0; base < B; base += 256) {
-    int n[8], sum = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) n[i] = pages_at(base + i * 32 + lane);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) sum += n[i];
-    total += warp_sum(sum);
-  }
-  const int chunk = total > 0 ? (total + prm.G - 1) / prm.G : 1;
-  const int start = min(total, unit * chunk), end = min(total, start + chunk);
-  int pb = 0, b0 = B, pb0 = total;
-  bool found = false;
-  for (int base = 0; base < B && !found; base += 256) {
-    int n[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) n[i] = pages_at(base + i * 32 + lane);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      if (found) break;
-      int incl = n[i];
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += v;
-      }
-      // the first sequence whose pages end past `start`; every earlier one ends at or before it
-      const int bb = base + i * 32 + lane;
-      const unsigned hit = __ballot_sync(0xffffffffu, bb < B && pb + incl > start);
-      if (hit) {
-        const int first = __ffs(hit) - 1;
-        b0 = base + i * 32 + first;
-        pb0 = pb + __shfl_sync(0xffffffffu, incl - n[i], first);
-        found = true;
-      } else {
-        pb += __shfl_sync(0xffffffffu, incl, 31);
-      }
-    }
-  }
-  if (lane == 0) *out = Plan{start, end, b0, pb0, chunk};
-}
-
-// Walks the (sequence, page range) segments of this CTA's work unit in order; every
-// role runs its own copy and sees the same sequence.
-struct Segments {
-  const int* lens;
-  int B, NQT, max_pages, start, end, b, pb;
-  __device__ void init(const Params& prm, const Plan& plan) {
-    lens = prm.cache_lens;
-    NQT = prm.NQT;
-    B = prm.B * prm.NQT;
-    max_pages = prm.max_pages;
-    start = plan.start;
-    end = plan.end;
-    b = plan.b0;
-    pb = plan.pb0;
-  }
-  // Next non-empty segment: sets seq (the virtual sequence: sequence * NQT + query tile),
-  // L, lo, hi (page indices within the sequence); flat0 = the sequence's first flat page.
-  // Lengths are fetched eight at a time so that skipping to this unit's first sequence
-  // costs one load latency per eight sequences rather than one per sequence.
-  int flat0 = 0;
-  __device__ bool next(int& seq, int& L, int& lo, int& hi) {
-    while (b < B && pb < end) {
-      int Ls[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) Ls[i] = b + i < B ? __ldg(lens + (b + i) / NQT) : 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if (b >= B || pb >= end) return false;
-        const int Lb = clamp_len(Ls[i], max_pages);
-        const int n = pages_of(Lb, kPage);
-        const int l0 = max(start, pb) - pb, h0 = min(end, pb + n) - pb;
-        const int cur = b, cur_pb = pb;
-        pb += n;
-        ++b;
-        if (l0 < h0) {
-          flat0 = cur_pb;
-          seq = cur;
-          L = Lb;
-          lo = l0;
-          hi = h0;
-          return true;
-        }
-      }
-    }
-    return false;
-  }
 };
 
 __device__ __forceinline__ int page_row(const Params& p, int vseq, int pg) {
@@ -767,10 +659,12 @@ __global__ void __launch_bounds__(256) zero_counters_kernel(int* __restrict__ c,
 
 // Makes the driver load every decode kernel on the current device (under lazy module loading
 // a kernel's module is otherwise loaded, and its device memory allocated, at its first launch).
+cudaError_t load_decode_t_kernels();
 cudaError_t load_decode_kernels() {
   using namespace sm103_decode;
   cudaFuncAttributes fa;
-  cudaError_t e;
+  cudaError_t e = load_decode_t_kernels();
+  if (e != cudaSuccess) return e;
   if ((e = cudaFuncGetAttributes(&fa, decode_split_kernel<false>)) != cudaSuccess) return e;
   if ((e = cudaFuncGetAttributes(&fa, decode_split_kernel<true>)) != cudaSuccess) return e;
   return cudaFuncGetAttributes(&fa, zero_counters_kernel);

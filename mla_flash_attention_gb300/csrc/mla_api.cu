@@ -2,6 +2,7 @@
 // device error word, decode workspace sizing and kernel dispatch.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
@@ -10,6 +11,7 @@
 #include <string>
 
 #include "../../include/mla.h"
+#include "../../include/mla_testing.h"
 #include "common.cuh"
 
 namespace mla {
@@ -28,6 +30,13 @@ cudaError_t launch_decode_sm103(const void* q_latent, const void* q_rope, const 
                                 int num_pages, float softmax_scale, int causal, bool fp8,
                                 float* part_o, float* part_lse, int* counters, void* out,
                                 float* lse, int G, unsigned int* err, cudaStream_t stream);
+cudaError_t launch_decode_t_sm103(const void* q_latent, const void* q_rope, const void* kv_cache,
+                                  const float* kv_scale, const int* page_table,
+                                  const int* cache_lens, int B, int H, int T, int max_pages,
+                                  int num_pages, float softmax_scale, int causal, float* part_o,
+                                  float* part_lse, int* counters, void* out, float* lse, int G,
+                                  unsigned int* err, long long wait_limit, int skip_unit,
+                                  cudaStream_t stream);
 cudaError_t launch_absorb_sm103(const void* x, const void* w, void* y, int R, int H, int K, int N,
                                 unsigned int* err, cudaStream_t stream);
 size_t prefill_bwd_workspace_bytes(int B, int H, int S);
@@ -89,9 +98,19 @@ int num_sms_current() {
   return n;
 }
 
-// Decode work units: each unit is served by a pair of CTAs (one per half of the latent
-// output columns), one CTA per SM.
+// Decode work units of the split kernel: each unit is served by a pair of CTAs (one per half
+// of the latent output columns), one CTA per SM.
 int decode_units() { return num_sms_current() / 2; }
+
+// The transposed decode kernel (one CTA per SM and work unit) serves an fp8 cache when a
+// sequence has at most 32 query rows (q_len * H).
+constexpr int kTransposedMaxRows = 32;
+bool decode_transposed(bool fp8, int TH) { return fp8 && TH <= kTransposedMaxRows; }
+
+// Test hooks (mla_testing.h): a decode launch of the transposed kernel leaves raw unit
+// `g_skip_unit` unloaded and gives each pipeline wait `g_wait_limit` SM clocks.
+std::atomic<int> g_skip_unit{-1};
+std::atomic<long long> g_wait_limit{1000000000LL};
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -120,6 +139,21 @@ DecodeWorkspace decode_workspace_layout(void* base, int B, int TH, int d_latent,
   return w;
 }
 
+// Workspace of the transposed kernel: G = SMs units, S = G + B slots of TQ = q_len*H rows:
+// O partials [S][TQ][d_latent] fp32, LSE partials [S][TQ] fp32, one split counter per sequence.
+DecodeWorkspace decode_workspace_layout_t(void* base, int B, int TH, int d_latent, int G) {
+  DecodeWorkspace w;
+  const size_t slots = (size_t)G + (size_t)B;
+  const size_t o_bytes = align_up(slots * TH * d_latent * sizeof(float), 256);
+  const size_t l_bytes = align_up(slots * TH * sizeof(float), 256);
+  const size_t c_bytes = align_up((size_t)B * sizeof(int), 256);
+  w.part_o = static_cast<float*>(base);
+  w.part_lse = reinterpret_cast<float*>(static_cast<char*>(base) + o_bytes);
+  w.counters = reinterpret_cast<int*>(static_cast<char*>(base) + o_bytes + l_bytes);
+  w.bytes = o_bytes + l_bytes + c_bytes;
+  return w;
+}
+
 }  // namespace
 
 namespace mla {
@@ -141,6 +175,11 @@ mla_status set_last_error(mla_status st, const char* fmt, ...) {
 extern "C" {
 
 const char* mla_last_error(void) { return g_last_error.c_str(); }
+
+void mla_testing_decode_stall(int skip_unit, long long wait_limit_cycles) {
+  g_skip_unit.store(skip_unit < 0 ? -1 : skip_unit);
+  g_wait_limit.store(wait_limit_cycles > 0 ? wait_limit_cycles : 1000000000LL);
+}
 
 int mla_version(void) { return 100; }
 
@@ -255,7 +294,10 @@ size_t mla_decode_workspace_size(int B, int H, int q_len, int d_latent) {
   if (B <= 0 || H <= 0 || q_len <= 0 || d_latent <= 0) return 0;
   const int G = decode_units();
   if (G <= 0) return 0;
-  return decode_workspace_layout(nullptr, B, H * q_len, d_latent, G).bytes;
+  size_t bytes = decode_workspace_layout(nullptr, B, H * q_len, d_latent, G).bytes;
+  if (decode_transposed(true, H * q_len))  // the size cannot depend on the cache type
+    bytes = std::max(bytes, decode_workspace_layout_t(nullptr, B, H * q_len, d_latent, 2 * G).bytes);
+  return bytes;
 }
 
 mla_status mla_decode(const void* q_latent, const void* q_rope, const void* kv_cache,
@@ -286,22 +328,28 @@ mla_status mla_decode(const void* q_latent, const void* q_rope, const void* kv_c
     return fail(MLA_ERR_UNSUPPORTED, "mla_decode: kv_dtype must be MLA_BF16 or MLA_FP8_E4M3");
   if (fp8 != (kv_scale != nullptr))
     return fail(MLA_ERR_INVALID_ARG, "mla_decode: kv_scale is required for fp8 and must be NULL for bf16");
-  const void* ptrs[] = {q_latent, q_rope, kv_cache, out, lse, workspace};
+  const void* ptrs[] = {q_latent, q_rope, kv_cache, kv_scale, out, lse, workspace};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return fail(MLA_ERR_INVALID_ARG, "mla_decode: tensors must be 16-byte aligned");
   const int G = decode_units();
   if (G <= 0) return fail(MLA_ERR_CUDA, "mla_decode: cannot query the SM count");
-  DecodeWorkspace ws = decode_workspace_layout(workspace, B, H * q_len, d_latent, G);
+  const bool tr = decode_transposed(fp8, H * q_len);
+  DecodeWorkspace ws = tr ? decode_workspace_layout_t(workspace, B, H * q_len, d_latent, 2 * G)
+                          : decode_workspace_layout(workspace, B, H * q_len, d_latent, G);
   if (!workspace || workspace_bytes < ws.bytes)
     return fail(MLA_ERR_WORKSPACE, "mla_decode: workspace of %zu bytes is smaller than the %zu needed",
                 workspace_bytes, ws.bytes);
   unsigned int* err = device_error_word();
   if (!err) return fail(MLA_ERR_CUDA, "mla_decode: device error word not reachable");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = mla::launch_decode_sm103(q_latent, q_rope, kv_cache, kv_scale, page_table,
-                                           cache_lens, B, H, q_len, max_pages_per_seq, num_pages,
-                                           softmax_scale, causal != 0, fp8, ws.part_o,
-                                           ws.part_lse, ws.counters, out, lse, G, err, st);
+  cudaError_t e =
+      tr ? mla::launch_decode_t_sm103(q_latent, q_rope, kv_cache, kv_scale, page_table, cache_lens, B, H,
+                                      q_len, max_pages_per_seq, num_pages, softmax_scale, causal != 0,
+                                      ws.part_o, ws.part_lse, ws.counters, out, lse, 2 * G, err,
+                                      g_wait_limit.load(), g_skip_unit.load(), st)
+         : mla::launch_decode_sm103(q_latent, q_rope, kv_cache, kv_scale, page_table, cache_lens, B, H,
+                                    q_len, max_pages_per_seq, num_pages, softmax_scale, causal != 0, fp8,
+                                    ws.part_o, ws.part_lse, ws.counters, out, lse, G, err, st);
   if (e != cudaSuccess) return cuda_fail(e, "mla_decode launch");
   return MLA_OK;
 }
