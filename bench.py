@@ -45,14 +45,58 @@ def decode_kv_bytes(inp):
     return float(inp.cache_lens.astype("int64").sum()) * per
 
 
+TENSOR_PEAKS = os.path.join(ROOT, "profiles", "tensor_peaks.json")
+
+
 def peaks():
+    """HBM and bf16 peaks from MEASURED_PEAKS.json (else the fallback figures); the fp8 dense
+    peak from profiles/tensor_peaks.json (written by --measure-tensor-peaks on a GB300), else
+    the nominal fp8:bf16 ratio of 2 times the bf16 peak."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
-                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
-    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
-            "source": "fallback"}
+        pk = {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+              "bf16_tflops_sustained": d.get("bf16_tflops_sustained"),
+              "peak_sm_mhz": (d.get("clocks_under_load") or {}).get("sm_mhz_median"),
+              "source": "measured"}
+    else:
+        pk = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+              "peak_sm_mhz": None, "source": "fallback"}
+    pk["fp8_tflops"], pk["fp8_source"] = 2.0 * pk["bf16_tflops"], "2 x bf16 (nominal ratio)"
+    if os.path.exists(TENSOR_PEAKS):
+        t = json.load(open(TENSOR_PEAKS))
+        if t.get("fp8_e4m3_tflops"):
+            pk["fp8_tflops"], pk["fp8_source"] = t["fp8_e4m3_tflops"], "measured (profiles/tensor_peaks.json)"
+    return pk
+
+
+def fp8_prefill_roofline(pairs, ms, pk):
+    """Both rooflines of the per-token-scale fp8 prefill.  Per visible (query, key) pair:
+    Q_nope K_nope' 2*128 FLOP and P V 2*128 FLOP with fp8 inputs, Q_rope K_rope' 2*64 FLOP in
+    bf16.  fp8-input roofline: the fp8 FLOP at the fp8 peak plus the rope FLOP at the bf16
+    peak.  Issued-precision roofline: as the kernel issues them -- nope scores on fp8, rope on
+    bf16, and P V as two bf16 products (the high and low bf16 parts of P' = p ks)."""
+    f_nope, f_rope, f_pv = 2.0 * 128 * pairs, 2.0 * 64 * pairs, 2.0 * 128 * pairs
+    t_in = (f_nope + f_pv) / (pk["fp8_tflops"] * 1e12) + f_rope / (pk["bf16_tflops"] * 1e12)
+    t_issued = f_nope / (pk["fp8_tflops"] * 1e12) + (f_rope + 2 * f_pv) / (pk["bf16_tflops"] * 1e12)
+    t = ms * 1e-3
+    return {"flop_split": {"fp8_nope_scores": f_nope, "bf16_rope_scores": f_rope, "fp8_pv": f_pv},
+            "roofline_ms_fp8_input": t_in * 1e3, "frac_fp8_input": t_in / t,
+            "roofline_ms_issued": t_issued * 1e3, "frac_issued": t_issued / t,
+            "target_ms_60pct_issued": t_issued * 1e3 / 0.6,
+            "peaks": {"fp8_tflops": pk["fp8_tflops"], "fp8_source": pk["fp8_source"],
+                      "bf16_tflops": pk["bf16_tflops"], "bf16_source": pk["source"]}}
+
+
+def clock_normalised(frac, clocks, pk):
+    """The roofline fraction per SM clock: frac x (clock of the peak measurement / clock of this
+    run), both the median SM clock under load.  The measured peaks ran power-capped at a lower
+    clock than this bench's kernels, so the plain fraction flatters a kernel that runs at the
+    maximum clock."""
+    if not clocks or not clocks.get("sm_mhz") or not pk.get("peak_sm_mhz"):
+        return None
+    return {"frac_per_clock": frac * pk["peak_sm_mhz"] / clocks["sm_mhz"],
+            "run_sm_mhz": clocks["sm_mhz"], "peak_run_sm_mhz": pk["peak_sm_mhz"]}
 
 
 def kernel_source_hash(files):
@@ -243,6 +287,11 @@ def run_gpu(args):
     barrier, max_over_ranks = ranks.barrier, ranks.max
 
     pk = peaks()
+    l2_buf = torch.empty(64 << 20, dtype=torch.float32, device=dev)  # 256 MB, about 2 x L2
+
+    def l2_flush():
+        l2_buf.zero_()
+
     # ---------------- headline: bf16 prefill
     inp = config_inputs(HEADLINE)
     t = prefill_to_device(inp, dev)
@@ -318,6 +367,7 @@ def run_gpu(args):
                   "schedule": "pinned host buffers; per batch element H2D / mla_prefill / D2H "
                               "pipelined over two copy streams"}
     res["clocks"] = clocks
+    res["roofline"]["clock_normalised"] = clock_normalised(res["roofline"]["frac"], clocks, pk)
 
     # ---------------- decode (bf16) and the fp8 workloads
     def decode_entry(name, with_append=False):
@@ -334,14 +384,22 @@ def run_gpu(args):
 
         barrier()
         dms = max_over_ranks(time_graph(call, args.steps, args.warmup))
+        # the same call timed one by one with L2 flushed before each (a 256 MB write outside
+        # the events): per-call events include the launch of the two kernels of a call
+        fms = max_over_ranks(statistics.mean(time_calls(call, args.steps, args.warmup, before=l2_flush)))
         kv = decode_kv_bytes(dinp)
         gbs = kv / (dms * 1e-3) / 1e9
         binding.check_device_error()
         res_d = {"workload": name, "ms": dms, "kv_bytes": kv, "kv_gbs": world * gbs,
                  "frac_hbm": gbs / pk["hbm_gbs"],
-                 "l2": "cache (%.0f MB) larger than L2; no flush" % (kv / 1e6),
-                 "timing": "CUDA graph of 10 calls replayed back to back between events",
-                 "launches_per_call": 1, "memsets_per_call": 1}
+                 "l2": "cache (%.0f MB) larger than L2" % (kv / 1e6),
+                 "timing": "CUDA graph of 10 calls replayed back to back between events (no flush)",
+                 "l2_flushed": {"ms": fms, "kv_gbs": world * kv / (fms * 1e-3) / 1e9,
+                                "frac_hbm": kv / (fms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                                "timing": "per-call CUDA events, 256 MB written before each call"},
+                 "launches_per_call": 2}
+        nonlocal launches
+        launches += 2 * (max(1, args.steps // 10) * 10 + args.steps)
         if with_append:
             # the step before decode: the q_len new rows of every sequence into the same cache
             c_new = torch.randn((dinp.B, dinp.T, dinp.d_latent + dinp.d_rope), device=dev).to(torch.bfloat16)
@@ -369,11 +427,12 @@ def run_gpu(args):
         pms = max_over_ranks(statistics.mean(time_calls(call, args.steps, args.warmup)))
         f = prefill_flops(pinp.B, pinp.H, pinp.S)
         tf = f / (pms * 1e-3) / 1e12
-        return {"workload": name, "ms": pms, "flops": f, "tflops": world * tf,
-                "frac_bf16_peak": tf / pk["bf16_tflops"], "out_dtype": "fp32"}
+        pairs = pinp.B * pinp.H * pinp.S * (pinp.S + 1) / 2
+        rl = fp8_prefill_roofline(pairs, pms, pk)
+        return {"workload": name, "ms": pms, "flops": f, "tflops": world * tf, "out_dtype": "fp32",
+                "roofline": {"bound": "tensor", "achieved": tf, "unit": "TFLOP/s", **rl}}
 
     res["decode"] = decode_entry(DECODE)
-    launches += args.steps * 1
 
     def backward_entry():
         # gradients of the headline prefill (B4 H128 S4096 causal) for a random upstream dO:
@@ -435,7 +494,7 @@ def run_gpu(args):
         f = 2.0 * pairs * (cinp.d_latent + cinp.d_rope + cinp.d_latent)
         return {"workload": "chunk of 64 new tokens on 4032 cached, B4 H128, bf16 cache",
                 "timing": "CUDA graph of 10 calls replayed back to back between events", "ms": cms, "flops_absorbed": f, "tflops": world * f / (cms * 1e-3) / 1e12,
-                "launches_per_call": 1, "memsets_per_call": 1}
+                "launches_per_call": 2}
 
     # the absorption products either side of the bf16 decode workload (B64 T1 H128)
     evict = torch.ones(64 << 20, dtype=torch.float32, device=dev)  # 256 MB, read to evict L2
@@ -459,9 +518,9 @@ def run_gpu(args):
     if not args.quick:
         res["prefill_fp8"] = prefill_entry(PREFILL_FP8)
         res["decode_fp8"] = decode_entry(DECODE_FP8, with_append=True)
-        launches += args.steps * 3  # fp8 prefill, fp8 decode, cache append
+        launches += args.steps * 1 + max(1, args.steps // 10) * 10  # fp8 prefill, cache append
         res["chunked_prefill"] = chunked_entry()
-        launches += args.steps * 1
+        launches += 2 * max(1, args.steps // 10) * 10
     res["gpu_launches"] = launches
     if rank == 0:
         res["cpu_baseline"] = cpu_baseline(inp_name=HEADLINE, budget_s=args.cpu_seconds)
@@ -583,6 +642,54 @@ def run_profile_case(name):
     binding.check_device_error()
 
 
+def measure_tensor_peaks():
+    """Dense library-GEMM peaks on cuda:0 (8192^3, best of 10 CUDA-event timings after warm-up;
+    clocks untouched and sampled): bf16 torch.matmul and fp8 e4m3 torch._scaled_mm with
+    bf16 output.  Writes profiles/tensor_peaks.json."""
+    import datetime
+
+    import torch
+
+    dev = torch.device("cuda", 0)
+    n = 8192
+    a = torch.randn((n, n), device=dev)
+    b = torch.randn((n, n), device=dev)
+    ab, bb = a.to(torch.bfloat16), b.to(torch.bfloat16)
+    a8 = (a / 4).to(torch.float8_e4m3fn)
+    b8 = (b / 4).to(torch.float8_e4m3fn).t()  # column-major operand
+    one = torch.tensor(1.0, device=dev)
+
+    def best(fn):
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(10):
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            fn()
+            e.record()
+            torch.cuda.synchronize()
+            ts.append(s.elapsed_time(e))
+        return min(ts)
+
+    with ClockSampler(0) as clk:
+        t_bf16 = best(lambda: torch.matmul(ab, bb))
+        t_fp8 = best(lambda: torch._scaled_mm(a8, b8, scale_a=one, scale_b=one, out_dtype=torch.bfloat16))
+    f = 2.0 * n ** 3
+    res = {"bf16_tflops": f / (t_bf16 * 1e-3) / 1e12, "fp8_e4m3_tflops": f / (t_fp8 * 1e-3) / 1e12,
+           "how": "torch.matmul bf16 and torch._scaled_mm e4m3 (bf16 out), %d^3, best of 10 CUDA-event "
+                  "timings after 5 warm-ups; clocks not changed" % n,
+           "command": "python bench.py --measure-tensor-peaks",
+           "clocks": clk.summary(), "torch": torch.__version__,
+           "gpu": torch.cuda.get_device_name(dev),
+           "when": datetime.datetime.now(datetime.timezone.utc).strftime("%Y-%m-%dT%H:%M:%SZ")}
+    os.makedirs(os.path.dirname(TENSOR_PEAKS), exist_ok=True)
+    with open(TENSOR_PEAKS, "w") as fh:
+        json.dump(res, fh, indent=1)
+    print(json.dumps(res))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--profile", choices=sorted(PROFILE_CASES),
@@ -593,7 +700,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--quick", action="store_true", help="headline prefill + bf16 decode only")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--measure-tensor-peaks", action="store_true",
+                    help="measure dense bf16 / fp8 library-GEMM peaks into profiles/tensor_peaks.json")
     args = ap.parse_args()
+    if args.measure_tensor_peaks:
+        measure_tensor_peaks()
+        return
     if args.profile:
         run_profile_case(args.profile)
         return

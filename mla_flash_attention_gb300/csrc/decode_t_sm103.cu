@@ -31,7 +31,8 @@
 //   warps 6-9   softmax (one thread per key of the block), P'' into shared memory; at the
 //               end of a sequence's segment the epilogue (one thread per latent row of O')
 //               and, in the CTA that completes a sequence, the merge of its splits
-// TMEM columns: [0, 4 NP) O' (four blocks of 128 latent rows), [4 NP, 6 NP) two S' buffers.
+// TMEM columns: [0, 4 NP) O' (four blocks of 128 latent rows), [4 NP, 6 NP) two S' buffers,
+// [6 NP, 7 NP) each softmax thread's part of the row sums (lane = the thread's key slot).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -71,8 +72,9 @@ struct Lay {
   static constexpr int kOffP = kOffRaw + kRawSlots * kRawUnit;
   static constexpr int kSmem = kOffP + 2 * kPBytes;
   static constexpr int kSmemAlloc = kSmem + 1024;
-  static constexpr int kTmemO = 0, kTmemS = 4 * NP;
-  static constexpr int kTmemCols = 6 * NP <= 128 ? 128 : 256;
+  // TMEM columns: O' (4 blocks of NP), two S' buffers, and the softmax threads' row-sum parts
+  static constexpr int kTmemO = 0, kTmemS = 4 * NP, kTmemL = 6 * NP;
+  static constexpr int kTmemCols = 7 * NP <= 128 ? 128 : 256;
   static constexpr uint32_t kPSwz = NP == 32 ? ptx::kSwz64 : ptx::kSwz32;
   static_assert(kOffWide % 1024 == 0 && kOffP % 1024 == 0, "operand tiles need 1 KB alignment");
   static_assert(kSmemAlloc <= 227 * 1024, "shared memory");
@@ -112,7 +114,7 @@ struct Bars {
   int abort_flag;
   int merge_last;
   Plan plan;
-  float qsc[2][32];     // per query row: scale * log2(e) * 2^-e of the row's Q scaling
+  __align__(16) float qsc[2][32];  // per query row: scale * log2(e) * 2^-e of its Q scaling
   float red[4][32];     // column reductions across the four softmax warps
   float colv[32];       // reduced columns
   float mref[32];       // reference of each query row (the same in every softmax thread)
@@ -580,7 +582,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int st = threadIdx.x - 192;       // 0..127
     bool ok = true;
-    float lp[NP];  // this thread's part of the row sums (its keys)
+    // this thread's part of the row sums (over the keys it has seen) lives in TMEM columns
+    // [kTmemL, kTmemL + NP) of its lane
+    const uint32_t lp_addr = tmem + lane_off + L_::kTmemL;
+    auto lp_ld = [&](int c, uint32_t (&v)[16]) { ptx::tmem_ld16(lp_addr + c, v); };
+    auto lp_st = [&](int c, const uint32_t (&v)[16]) { ptx::tmem_st16(lp_addr + c, v); };
+    // the rows' references, the same in every softmax thread, live in registers; the rows' score
+    // scales are read once per block as 16-byte vectors (the shared-memory queue is busy with
+    // the widening, so few and independent loads)
+    float m[NP];
     // Group barrier of the four softmax warps on an mbarrier (bounded wait, so that a warp that
     // gave up cannot leave the others waiting forever).  Every warp passes the same sequence of
     // barriers, so the phase of barrier number n is n & 1.
@@ -600,33 +610,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = st; i < TH * (kDl / 8); i += 128) o[i] = make_uint4(0, 0, 0, 0);
       for (int i = st; i < TH; i += 128) p.lse[((size_t)b * p.H + i % p.H) * p.T + i / p.H] = -INFINITY;
     }
-    // key scales one block ahead
-    BlockIter ahead;
-    ahead.init(p, bars.plan);
-    Block nb;
+    // key scales one block ahead (the iterator already holds the next block and its pages)
     auto fetch_ks = [&](const Block& bb) -> float {
       const int q = kq >> 6, r = kq & 63;
       int ph;
       const int v = valid_rows(p, bb, q, &ph);
       return r < v ? __ldg(p.kv_scale + (size_t)ph * kPage + r) : 0.f;
     };
-    float ks_next = ahead.next(nb) ? fetch_ks(nb) : 0.f;
+    float ks_next = it.has ? fetch_ks(it.nxt) : 0.f;
     int n_epi = 0;
     while (ok && it.next(cur)) {
       const float ks_raw = ks_next;
-      if (ahead.next(nb)) ks_next = fetch_ks(nb);
+      if (it.has) ks_next = fetch_ks(it.nxt);
       if (cur.first) {
         if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.qsc_full[cur.seg & 1], (cur.seg >> 1) & 1,
                                                           abort_flag, p.err, lim))))
           break;
 #pragma unroll
-        for (int q = 0; q < NP; ++q) lp[q] = 0.f;
-        // a segment starts without references; only thread st uses column st before the next
-        // group barrier (every thread has finished the previous segment's epilogue by now)
-        if (st < NP) bars.mref[st] = -INFINITY;
+        for (int q = 0; q < NP; ++q) m[q] = -INFINITY;
+        uint32_t z[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) z[i] = 0u;
+#pragma unroll
+        for (int c = 0; c < NP; c += 16) lp_st(c, z);
+        ptx::tmem_st_wait();
       }
-      const float* qs = bars.qsc[cur.seg & 1];  // released at the end of the segment
-      const float* m = bars.mref;
       // this thread's key; a zero scale is raised to 2^-64 (its key and value are then ~0 but
       // its probability still counts in the row sum)
       const int half = kq >> 6, r64 = kq & 63;
@@ -655,6 +663,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // u = t + log2(ks) with t = scale * ks * s (the log2-domain score); invisible keys and
       // padding rows -inf
       const int vis_all = p.causal ? cur.L - p.T : cur.L - 1;  // keys <= this are seen by every row
+      float qs[NP];
+#pragma unroll
+      for (int q = 0; q < NP; q += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(&bars.qsc[cur.seg & 1][q]);
+        qs[q] = v.x;
+        qs[q + 1] = v.y;
+        qs[q + 2] = v.z;
+        qs[q + 3] = v.w;
+      }
       bool grow = false;
 #pragma unroll
       for (int q = 0; q < NP; ++q) {
@@ -682,29 +699,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (lane < NP) bars.red[warp & 3][lane] = wmax;
         if (!(ok = group_sync())) break;
-        if (st < NP) {
-          const float cm = fmaxf(fmaxf(bars.red[0][st], bars.red[1][st]), fmaxf(bars.red[2][st], bars.red[3][st]));
-          const float mo = bars.mref[st], mn = fmaxf(mo, cm);
-          bars.alpha[st] = (mo == -INFINITY || mn == -INFINITY) ? 1.f : ptx::ex2(mo - mn);
-          bars.mref[st] = mn;
-        }
+        if (st < NP)
+          bars.colv[st] = fmaxf(fmaxf(bars.red[0][st], bars.red[1][st]), fmaxf(bars.red[2][st], bars.red[3][st]));
         if (!(ok = group_sync())) break;
-        const float* alpha = bars.alpha;
+        // new references; the rescale factors go to shared memory (read by the O' rescale)
         bool shrink = false;
 #pragma unroll
-        for (int q = 0; q < NP; ++q) shrink = shrink || alpha[q] != 1.f;
+        for (int q = 0; q < NP; ++q) {
+          const float mn = fmaxf(m[q], bars.colv[q]);
+          const float al = (m[q] == -INFINITY || mn == -INFINITY) ? 1.f : ptx::ex2(m[q] - mn);
+          shrink = shrink || al != 1.f;
+          if (st == q) bars.alpha[q] = al;
+          m[q] = mn;
+        }
+        const float* alpha = bars.alpha;
         if (!cur.first && shrink) {
           // O' holds the contributions of this segment's earlier blocks (PV(j-1) included):
-          // scale its columns, and the row sums, to the new references
+          // scale its columns, and the row sums, to the new references (16 columns at a time:
+          // the scores stay live in registers meanwhile)
           if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.o_done, (cur.j - 1) & 1, abort_flag, p.err, lim))))
             break;
           ptx::tc_fence_after();
-#pragma unroll
-          for (int q = 0; q < NP; ++q) lp[q] *= alpha[q];
-          // (16 columns at a time: u and the row sums stay live in registers meanwhile)
 #pragma unroll 1
-          for (int c0 = 0; c0 < 4 * NP; c0 += 16) {
+          for (int c1 = 0; c1 < 5 * NP; c1 += 16) {
             uint32_t ov[16];
+            const int c0 = c1 < 4 * NP ? c1 : L_::kTmemL + (c1 - 4 * NP);  // O' blocks, then the sums
             const uint32_t oa = tmem + lane_off + L_::kTmemO + c0;
             ptx::tmem_ld16(oa, ov);
             ptx::tmem_ld_wait();
@@ -720,13 +739,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       // P'' = exp2(u - m) (f16, <= 2^kTau), and the row sums of P'' / ks = exp2(t - m)
       uint32_t pk[NP / 2];
 #pragma unroll
-      for (int q = 0; q < NP; q += 2) {
-        const float a = ptx::ex2(u[q] - (m[q] == -INFINITY ? 0.f : m[q]));
-        const float b = ptx::ex2(u[q + 1] - (m[q + 1] == -INFINITY ? 0.f : m[q + 1]));
-        lp[q] = fmaf(a, inv_ks, lp[q]);
-        lp[q + 1] = fmaf(b, inv_ks, lp[q + 1]);
-        pk[q / 2] = ptx::pack_f16x2(a, b);
+      for (int c = 0; c < NP; c += 16) {
+        uint32_t lv[16];
+        lp_ld(c, lv);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int q = c; q < c + 16; q += 2) {
+          const float a = ptx::ex2(u[q] - (m[q] == -INFINITY ? 0.f : m[q]));
+          const float b = ptx::ex2(u[q + 1] - (m[q + 1] == -INFINITY ? 0.f : m[q + 1]));
+          lv[q - c] = __float_as_uint(fmaf(a, inv_ks, __uint_as_float(lv[q - c])));
+          lv[q + 1 - c] = __float_as_uint(fmaf(b, inv_ks, __uint_as_float(lv[q + 1 - c])));
+          pk[q / 2] = ptx::pack_f16x2(a, b);
+        }
+        lp_st(c, lv);
       }
+      ptx::tmem_st_wait();
       if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.p_free[cur.j & 1], ((cur.j >> 1) & 1) ^ 1, abort_flag, p.err, lim))))
         break;
       {
@@ -748,7 +775,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++n_epi;
       ptx::tc_fence_after();
       {
-        const float wsum = warp_column_sums<NP>(lp);  // (lp is rebuilt at the next segment)
+        float lp[NP];
+#pragma unroll
+        for (int c = 0; c < NP; c += 16) {
+          uint32_t lv[16];
+          lp_ld(c, lv);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) lp[c + i] = __uint_as_float(lv[i]);
+        }
+        const float wsum = warp_column_sums<NP>(lp);
         if (lane < NP) bars.red[warp & 3][lane] = wsum;
       }
       if (!(ok = group_sync())) break;
@@ -785,7 +821,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&bars.o_free);  // O' may be overwritten
       if (st < TQ) {
-        const float mq = bars.mref[st];
+        float mq = 0.f;
+#pragma unroll
+        for (int q = 0; q < NP; ++q) mq = q == st ? m[q] : mq;
         const float l = bars.colv[st];
         const float ls = l > 0.f ? (mq + __log2f(l)) * 0.69314718055994531f : -INFINITY;
         if (whole)

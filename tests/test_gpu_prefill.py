@@ -68,27 +68,26 @@ def test_extreme_scales(lib):
         check(o, O, l, L, TOL_O_BF16, what="scale %g" % sc)
 
 
-def _sampled(lib, name, tol, bf16_out):
+def _full_rows(lib, name, tol, bf16_out):
+    """Every output row of twelve (batch, head) pairs of a full-size workload -- the first and
+    the last pair and ten drawn ones -- against the oracle (the kernel orders its row blocks
+    longest first and skips tiles above the diagonal, so whole rows at full size are checked)."""
     inp = config_inputs(name)
     o, l = run(lib, inp)
     assert np.isfinite(o).all() and np.isfinite(l).all()
     rng = np.random.default_rng(7)
-    S = inp.S
-    rows = np.unique(np.concatenate([[0, 1, 63, 64, 127, 128, 255, 256, S - 129, S - 128, S - 1],
-                                     rng.integers(0, S, 21)]))
     pairs = [(0, 0), (inp.B - 1, inp.H - 1)] + [(int(rng.integers(inp.B)), int(rng.integers(inp.H)))
-                                               for _ in range(4)]
+                                               for _ in range(10)]
     for b, h in pairs:
-        O, L = oracle.prefill_bh(inp, b, h, rows)
-        check(o[b, rows, h], O, l[b, h, rows], L, tol, bf16_out=bf16_out,
-              what="%s b=%d h=%d" % (name, b, h))
+        O, L = oracle.prefill_bh(inp, b, h)
+        check(o[b, :, h], O, l[b, h], L, tol, bf16_out=bf16_out, what="%s b=%d h=%d" % (name, b, h))
 
 
 @pytest.mark.slow
-def test_full_size_bf16_sampled(lib):
-    _sampled(lib, "prefill_b4h128s4096_bf16", TOL_O_BF16, True)
+def test_full_size_bf16_every_row_of_twelve_heads(lib):
+    _full_rows(lib, "prefill_b4h128s4096_bf16", TOL_O_BF16, True)
 
 
 @pytest.mark.slow
-def test_full_size_fp8_sampled(lib):
-    _sampled(lib, "prefill_b2h128s8192_fp8", TOL_O_FP8, False)
+def test_full_size_fp8_every_row_of_twelve_heads(lib):
+    _full_rows(lib, "prefill_b2h128s8192_fp8", TOL_O_FP8, False)
