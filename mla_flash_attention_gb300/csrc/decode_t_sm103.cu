@@ -104,6 +104,7 @@ struct Params {
 
 struct Bars {
   uint64_t raw_full[kRawSlots], raw_empty[kRawSlots];
+  uint64_t raw_issued[kRawSlots];  // the producer has waited for the slot and issued its unit
   uint64_t wide_full[kWideSlots], wide_empty[kWideSlots];
   uint64_t q_free, q_ready;
   uint64_t qsc_full[2], qsc_free[2];
@@ -237,6 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kRawSlots; ++i) {
       ptx::mbar_init(&bars.raw_full[i], 1);
       ptx::mbar_init(&bars.raw_empty[i], 1);
+      ptx::mbar_init(&bars.raw_issued[i], 1);
     }
     for (int i = 0; i < kWideSlots; ++i) {
       ptx::mbar_init(&bars.wide_full[i], 1);
@@ -302,11 +304,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // one raw unit of 8 KB: score units take two 64 x 64 boxes (page a, then page b, at
     // cache column c); value units one 128 x 64 box (page a, columns c .. c + 127).  A page
     // of -1 is not loaded (its rows are zeroed by the widening).
+    // marks a slot's unit as handed out.  A widening warp can reach unit u before unit
+    // u - kRawSlots has landed (its own previous unit is u - 4), and a raw_full parity only
+    // names unit u once that has happened; it waits on raw_issued first, whose phase can be
+    // at most one behind (the producer has handed out u - 4, hence u - kRawSlots).
+    auto publish = [&](int slot) {
+      if (lane == 0) ptx::mbar_arrive(&bars.raw_issued[slot]);
+    };
     auto load = [&](bool score, int pa, int pb, int c) -> bool {
       const int slot = u % kRawSlots;
       if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bars.raw_empty[slot], ((u / kRawSlots) & 1) ^ 1, abort_flag, p.err, lim)))
         return false;
       if (u == p.skip_unit) {  // test hook: this unit's bytes never arrive
+        publish(slot);
         ++u;
         return true;
       }
@@ -321,6 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tma_load_2d(dst, &tm_v, &bars.raw_full[slot], c, pa * kPage);
       }
       last_unit = u;
+      publish(slot);
       ++u;
       return true;
     };
@@ -493,6 +504,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int mine = (u & 3) == wl;
       const int rs = u % kRawSlots, ws = u % kWideSlots;
       if (mine) {
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bars.raw_issued[rs], (u / kRawSlots) & 1, abort_flag, p.err, lim)))
+          return false;
         if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bars.raw_full[rs], (u / kRawSlots) & 1, abort_flag, p.err, lim)))
           return false;
         if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bars.wide_empty[ws], ((u / kWideSlots) & 1) ^ 1, abort_flag, p.err, lim)))
