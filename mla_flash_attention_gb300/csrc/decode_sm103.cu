@@ -57,6 +57,21 @@ constexpr int kQChunk = kRows * 128;          // 128 rows x 64 bf16 (16 KB)
 constexpr int kOffQhi = 0;                    // latent 256..511 (4 chunks) + rope (1 chunk)
 constexpr int kOffStage = 5 * kQChunk;        // 80 KB
 constexpr int kSmemBytes = kOffStage + kStages * kStageBytes;  // 224 KB
+// bf16 pages arrive in two parts: the score-only chunks (the other column half's four latent
+// chunks and the rope chunk, 40 KB) into one slot, free again once the score MMAs that read
+// them are done, and this CTA's own four latent chunks (32 KB), which the PV product reads
+// too, into a ring of three, so that they land two pages ahead of their use.
+constexpr int kSPartBytes = 5 * kPageChunk;
+constexpr int kVPartBytes = 4 * kPageChunk;
+constexpr int kVSlots = 3;
+constexpr int kOffSPart = kOffStage;
+constexpr int kOffVPart = kOffStage + kSPartBytes;
+static_assert(kOffVPart + kVSlots * kVPartBytes <= kSmemBytes, "bf16 page parts fit the stages");
+// position of 64-column chunk c (0..8) within its part, for column half `half`: the value
+// chunks 4 half .. 4 half + 3 in order; the score-only ones (half 0: 4..8, half 1: 0..3, 8)
+__host__ __device__ constexpr int chunk_idx(int c, int half) {
+  return ((c >> 2) == half && c < 8) ? c - 4 * half : (half == 0 ? c - 4 : (c < 4 ? c : 4));
+}
 constexpr int kSmemAlloc = kSmemBytes + 1024;
 // bf16: 8 warps; fp8: 12 (four more page-widening warps)
 template <bool kFp8> constexpr int kThreadsOf = kFp8 ? 384 : 256;
@@ -79,16 +94,25 @@ struct Params {
   int NQT, TQ;  // query tiles per sequence (T*H rows in tiles of 128) and rows per tile
   int n_slots;  // partial slots: G + B * NQT
   float scale_log2;
+  int page_box;  // 1: a page is one box of the 3-D cache map (else nine boxes of the 2-D one)
 };
 
 struct Bars {
   // stage_ready[s][k]: bf16 pages are ready at once (k = 0); fp8 pages in three parts, k = 0..2
   // covering 64-column chunks 3k..3k+2, as the in-place widening completes them
   uint64_t stage_full[kStages], stage_ready[kStages][3], stage_empty[kStages];
+  // bf16 page parts: the score-only slot and the ring of this half's value chunks; a page
+  // that ends a sequence part-way is handed to the preparation warps (zero_go) and back once
+  // the rows past the end are zeroed (zeroed), one phase each per such page
+  uint64_t spart_full, spart_empty;
+  uint64_t vpart_full[kVSlots], vpart_empty[kVSlots];
+  uint64_t zero_go, zeroed;
   uint64_t s_full[2], p_full[2], o_done, seg_done, conv_sync;
   uint64_t q_free, q_lo_full, q_cp_done, q_hi_full;  // per-sequence Q staging
+  uint64_t q0_copied;  // the first sequence's staged Q is in TMEM (one phase per launch)
   uint64_t part_done, merge_go;  // partial written by the 4 softmax warps / merge decision
-  int merge_last;
+  uint64_t dec_go;               // the segment's merge path decided
+  int merge_last, merge_fast;
   uint32_t tmem_base;
   int abort_flag;
   Plan plan;
@@ -104,6 +128,9 @@ __device__ __forceinline__ int page_row(const Params& p, int vseq, int pg) {
 template <bool kFp8>
 __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_cache,
+                        const __grid_constant__ CUtensorMap tm_page,
+                        const __grid_constant__ CUtensorMap tm_c4,
+                        const __grid_constant__ CUtensorMap tm_c5,
                         const __grid_constant__ CUtensorMap tm_qlat,
                         const __grid_constant__ CUtensorMap tm_qrope, const Params p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -116,7 +143,15 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
   // softmax, warps 4 + n_soft .. 7 join the preparation warps (2-3 and 8-11)
   const int n_soft = kFp8 ? (p.TQ + 31) / 32 : kRows / 32;
   const int n_prep = kPrepOf<kFp8> + (kFp8 ? 32 * (kRows / 32 - n_soft) : 0);
-  constexpr int kParts = kFp8 ? 3 : 1;  // readiness parts of a page stage
+  // readiness parts of a page stage: fp8 three groups of three widened chunks; bf16 the
+  // score-only part, then the value part
+  constexpr int kParts = kFp8 ? 3 : 2;
+  // the first sequence's Q latent 0..255 (four 16 KB chunks) is staged where pages 1 (fp8)
+  // or 1 and 2 (bf16: value slots 1 and 2) land
+  auto q_stage_off = [&](int c) -> int {
+    if constexpr (kFp8) return kOffStage + kStageBytes + c * kQChunk;
+    return kOffVPart + (1 + (c >> 1)) * kVPartBytes + (c & 1) * kQChunk;
+  };
   const int warp = threadIdx.x >> 5;
   const int unit = blockIdx.x >> 1, half = blockIdx.x & 1;
   const int TH = p.T * p.H, TQ = p.TQ;
@@ -130,6 +165,14 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
       for (int k = 0; k < 3; ++k) ptx::mbar_init(&bars.stage_ready[s][k], n_prep / 32);
       ptx::mbar_init(&bars.stage_empty[s], 1);
     }
+    ptx::mbar_init(&bars.spart_full, 1);
+    ptx::mbar_init(&bars.spart_empty, 1);
+    for (int v = 0; v < kVSlots; ++v) {
+      ptx::mbar_init(&bars.vpart_full[v], 1);
+      ptx::mbar_init(&bars.vpart_empty[v], 1);
+    }
+    ptx::mbar_init(&bars.zero_go, 1);
+    ptx::mbar_init(&bars.zeroed, n_prep / 32);
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&bars.s_full[i], 1);
       ptx::mbar_init(&bars.p_full[i], n_soft);  // one arrival per softmax warp
@@ -140,9 +183,11 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
     ptx::mbar_init(&bars.q_lo_full, 1);
     ptx::mbar_init(&bars.q_cp_done, 1);
     ptx::mbar_init(&bars.q_hi_full, 1);
+    ptx::mbar_init(&bars.q0_copied, 1);
     ptx::mbar_init(&bars.conv_sync, n_prep / 32);  // one arrival per preparation warp
     ptx::mbar_init(&bars.part_done, n_soft);
     ptx::mbar_init(&bars.merge_go, 1);
+    ptx::mbar_init(&bars.dec_go, 1);
     ptx::fence_barrier_init();
   }
   // Q rows T*H..127 are never loaded: keep them zero (finite scores in the padded rows)
@@ -162,47 +207,98 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
 
   if (warp == 0) {
     // -------------------------------------------------------------- TMA producer
-    if (ptx::elect_one()) {
+    // One lane issues Q, the pages in order (fp8: whole pages; bf16: the score-only part, then
+    // the value part, which is released later) and the L2 warming.  Copies are served in
+    // issue order, so a page's value part never waits behind the next page's score-only part.
+    if ((threadIdx.x & 31) == 0) {
       ptx::prefetch_tensormap(&tm_cache);
       ptx::prefetch_tensormap(&tm_qlat);
       int g = 0, nseg = 0;
       bool ok = true;
-      const int chunk_bytes = kFp8 ? kRawChunk : kPageChunk;
       while (ok && segs.next(seq, L, lo, hi)) {
-        if (nseg == 0) {
-          // first sequence: Q latent 0..255 staged in the (still unused) second page stage,
-          // the rest of Q straight into the Q area, all at once
-          ptx::mbar_arrive_expect_tx(&bars.q_lo_full, 4 * TQ * 128);
-          for (int c = 0; c < 4; ++c)
-            ptx::tma_load_2d(sm + kOffStage + kStageBytes + c * kQChunk, &tm_qlat, &bars.q_lo_full, c * 64, q_row0(seq));
-          ptx::mbar_arrive_expect_tx(&bars.q_hi_full, 5 * TQ * 128);
-          for (int c = 0; c < 4; ++c)
-            ptx::tma_load_2d(sm + kOffQhi + c * kQChunk, &tm_qlat, &bars.q_hi_full, 256 + c * 64, q_row0(seq));
-          ptx::tma_load_2d(sm + kOffQhi + 4 * kQChunk, &tm_qrope, &bars.q_hi_full, 0, q_row0(seq));
-        } else {
-          // Q latent 0..255 into the Q area once the previous sequence's last S is done
-          if (!(ok = ptx::mbar_wait(&bars.q_free, (nseg - 1) & 1, abort_flag, p.err))) break;
-          ptx::mbar_arrive_expect_tx(&bars.q_lo_full, 4 * TQ * 128);
-          for (int c = 0; c < 4; ++c)
-            ptx::tma_load_2d(sm + kOffQhi + c * kQChunk, &tm_qlat, &bars.q_lo_full, c * 64, q_row0(seq));
+        {
+          if (nseg == 0) {
+            // first sequence: Q latent 0..255 staged in the (still unused) second page
+            // stage, the rest of Q straight into the Q area, all at once
+            ptx::mbar_arrive_expect_tx(&bars.q_lo_full, 4 * TQ * 128);
+            for (int c = 0; c < 4; ++c)
+              ptx::tma_load_2d(sm + q_stage_off(c), &tm_qlat, &bars.q_lo_full, c * 64, q_row0(seq));
+            ptx::mbar_arrive_expect_tx(&bars.q_hi_full, 5 * TQ * 128);
+            for (int c = 0; c < 4; ++c)
+              ptx::tma_load_2d(sm + kOffQhi + c * kQChunk, &tm_qlat, &bars.q_hi_full, 256 + c * 64, q_row0(seq));
+            ptx::tma_load_2d(sm + kOffQhi + 4 * kQChunk, &tm_qrope, &bars.q_hi_full, 0, q_row0(seq));
+          } else {
+            // Q latent 0..255 into the Q area once the previous sequence's last S is done
+            if (!(ok = ptx::mbar_wait(&bars.q_free, (nseg - 1) & 1, abort_flag, p.err))) break;
+            ptx::mbar_arrive_expect_tx(&bars.q_lo_full, 4 * TQ * 128);
+            for (int c = 0; c < 4; ++c)
+              ptx::tma_load_2d(sm + kOffQhi + c * kQChunk, &tm_qlat, &bars.q_lo_full, c * 64, q_row0(seq));
+          }
+          ++nseg;
+          {  // warm L2 with the next segment's Q, read when this one's pages are done
+            Segments nx = segs;
+            int s2, L2, lo2, hi2;
+            if (nx.next(s2, L2, lo2, hi2)) {
+              const int r0 = q_row0(s2), rows = min(TQ, p.B * TH - r0);
+              if (rows > 0) {
+                ptx::bulk_prefetch(p.q_latent + (size_t)r0 * kDl, rows * kDl * 2);
+                ptx::bulk_prefetch(p.q_rope + (size_t)r0 * 64, rows * 128);
+              }
+            }
+          }
         }
-        ++nseg;
         for (int pg = lo; pg < hi; ++pg, ++g) {
           const int s = g % kStages;
-          if (!(ok = ptx::mbar_wait(&bars.stage_empty[s], ((g / kStages) & 1) ^ 1, abort_flag, p.err))) break;
-          // the second stage holds the first sequence's staged Q until it is copied to TMEM
-          // (when page 1 belongs to a later sequence, that sequence's wait for q_free
-          // already implied the copy: it precedes the first sequence's MMAs)
-          if (g == 1 && nseg == 1 && !(ok = ptx::mbar_wait(&bars.q_cp_done, 0, abort_flag, p.err))) break;
+          if (!(ok = ptx::mbar_wait(kFp8 ? &bars.stage_empty[s] : &bars.spart_empty,
+                                    kFp8 ? ((g / kStages) & 1) ^ 1 : (g & 1) ^ 1, abort_flag, p.err)))
+            break;
+          // the first sequence's staged Q stays in place until it is copied to TMEM
+          if (kFp8 && g == 1 && !(ok = ptx::mbar_wait(&bars.q0_copied, 0, abort_flag, p.err))) break;
           const int y = page_row(p, seq, pg);
-          unsigned char* dst = sm + kOffStage + s * kStageBytes + (kFp8 ? kRawOffset : 0);
-          ptx::mbar_arrive_expect_tx(&bars.stage_full[s], 9 * chunk_bytes);
-          for (int c = 0; c < 9; ++c)
-            ptx::tma_load_2d(dst + c * chunk_bytes, &tm_cache, &bars.stage_full[s], c * 64, y);
+          if constexpr (kFp8) {
+            unsigned char* dst = sm + kOffStage + s * kStageBytes + kRawOffset;
+            ptx::mbar_arrive_expect_tx(&bars.stage_full[s], 9 * kRawChunk);
+            if (p.page_box) {
+              ptx::tma_load_3d(dst, &tm_page, &bars.stage_full[s], 0, y, 0);
+            } else {
+              for (int c = 0; c < 9; ++c)
+                ptx::tma_load_2d(dst + c * kRawChunk, &tm_cache, &bars.stage_full[s], c * 64, y);
+            }
+          } else {
+            // score-only chunks in chunk_idx order: half 0 takes 4..8, half 1 0..3 and 8
+            unsigned char* dst = sm + kOffSPart;
+            ptx::mbar_arrive_expect_tx(&bars.spart_full, kSPartBytes);
+            if (p.page_box && half == 0) {
+              ptx::tma_load_3d(dst, &tm_c5, &bars.spart_full, 0, y, 4);
+            } else if (p.page_box) {
+              ptx::tma_load_3d(dst, &tm_c4, &bars.spart_full, 0, y, 0);
+              ptx::tma_load_2d(dst + 4 * kPageChunk, &tm_cache, &bars.spart_full, 512, y);
+            } else {
+              for (int i = 0; i < 5; ++i)
+                ptx::tma_load_2d(dst + i * kPageChunk, &tm_cache, &bars.spart_full,
+                                 (half == 0 ? 4 + i : (i < 4 ? i : 8)) * 64, y);
+            }
+            // own latent chunks 4 half .. 4 half + 3, once the page three back has had its PV
+            // (value slots 1 and 2 first hold the first sequence's staged Q)
+            const int v = g % kVSlots;
+            if (!(ok = ptx::mbar_wait(&bars.vpart_empty[v], ((g / kVSlots) & 1) ^ 1, abort_flag, p.err))) break;
+            if ((g == 1 || g == 2) && !(ok = ptx::mbar_wait(&bars.q0_copied, 0, abort_flag, p.err))) break;
+            dst = sm + kOffVPart + v * kVPartBytes;
+            ptx::mbar_arrive_expect_tx(&bars.vpart_full[v], kVPartBytes);
+            if (p.page_box) {
+              ptx::tma_load_3d(dst, &tm_c4, &bars.vpart_full[v], 0, y, 4 * half);
+            } else {
+              for (int c = 0; c < 4; ++c)
+                ptx::tma_load_2d(dst + c * kPageChunk, &tm_cache, &bars.vpart_full[v], (4 * half + c) * 64, y);
+            }
+          }
           // warm L2 with the pages ahead (after this page's own load has been issued)
           for (int a = (pg == lo ? lo + 1 : pg + kPrefetchAhead); a <= min(hi - 1, pg + kPrefetchAhead); ++a) {
             const int ya = page_row(p, seq, a);
-            if (ya >= 0)
+            if (ya < 0) continue;
+            if (p.page_box)
+              ptx::tma_prefetch_3d(&tm_page, 0, ya, 0);
+            else
               for (int c = 0; c < 9; ++c) ptx::tma_prefetch_2d(&tm_cache, c * 64, ya);
           }
         }
@@ -217,34 +313,76 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
       const uint32_t stage0 = ptx::smem_u32(sm + kOffStage);
       const uint32_t o_tm = tmem + 256;
       int g = 0, nseg = 0;
+      int n_zeroed = 0;  // bf16: partial pages zeroed so far
       bool ok = true;
-      // part `part` of S(gg): all 36 k-steps (bf16), or k-steps 12 part .. 12 part + 11 (fp8)
+      const uint32_t smb = ptx::smem_u32(sm);
+      // Operand descriptors, built once (k-step j of a chunk is 32 bytes further, i.e. 2 in
+      // the start-address field; a chunk 8 KB, i.e. 512): B = the page chunks (fp8: stage 0 /
+      // 1 in chunk order; bf16: the score-only slot, value slot 0 / 1 / 2), A = the shared-
+      // memory Q chunks.  This keeps the issue loop at an add or two per MMA: the MMA thread
+      // shares its SM sub-partition with a softmax warp.
+      const uint64_t b0 = ptx::sw128_desc(smb + (kFp8 ? kOffStage : kOffSPart), 16, 1024);
+      const uint64_t b1 = ptx::sw128_desc(smb + (kFp8 ? kOffStage + kStageBytes : kOffVPart), 16, 1024);
+      const uint64_t b2 = ptx::sw128_desc(smb + kOffVPart + kVPartBytes, 16, 1024);
+      const uint64_t b3 = ptx::sw128_desc(smb + kOffVPart + 2 * kVPartBytes, 16, 1024);
+      const uint64_t qd = ptx::sw128_desc(qhi, 16, 1024);
+      // k-step k (a compile-time constant at every call) of S into d, B from chunk base bc
+      auto mma_k = [&](uint32_t d, uint64_t bc, int k, bool acc) {
+        const uint64_t db = bc + 2 * (k & 3);
+        if (k < 16)  // latent 0..255: A from TMEM
+          ptx::mma_bf16_ts(d, tmem + k * 8, db, kIdS, acc ? 1u : 0u);
+        else         // latent 256..511 + rope: A from shared memory (16 KB per Q chunk)
+          ptx::mma_bf16_ss(d, qd + 1024 * ((k - 16) >> 2) + 2 * ((k - 16) & 3), db, kIdS, acc ? 1u : 0u);
+      };
+      // part `part` of S(gg): fp8 k-steps 12 part .. 12 part + 11; bf16 the k-steps of the
+      // score-only chunks (part 0), then those of the value chunks (part 1).  The first MMA
+      // of S(gg) starts the accumulator.
       auto issue_s = [&](int gg, int part) {
-        const uint32_t st = stage0 + (gg % kStages) * kStageBytes;
         const uint32_t d = tmem + 128 + (gg & 1) * 64;
+        if constexpr (kFp8) {
+          const uint64_t st = (gg % kStages) ? b1 : b0;
+          if (part == 0) {
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {  // latent 0..255: A from TMEM
-          if (kFp8 && k / 12 != part) continue;
-          const uint64_t db = ptx::sw128_desc(st + (k >> 2) * kPageChunk + (k & 3) * 32, 16, 1024);
-          ptx::mma_bf16_ts(d, tmem + k * 8, db, kIdS, k > 0);
-        }
+            for (int k = 0; k < 12; ++k) mma_k(d, st + 512 * (k >> 2), k, k > 0);
+          } else if (part == 1) {
 #pragma unroll
-        for (int k = 16; k < 36; ++k) {  // latent 256..511 + rope: A from shared memory
-          if (kFp8 && k / 12 != part) continue;
-          const int kq = k - 16;
-          const uint64_t da = ptx::sw128_desc(qhi + (kq >> 2) * kQChunk + (kq & 3) * 32, 16, 1024);
-          const uint64_t db = ptx::sw128_desc(st + (k >> 2) * kPageChunk + (k & 3) * 32, 16, 1024);
-          ptx::mma_bf16_ss(d, da, db, kIdS, 1);
+            for (int k = 12; k < 24; ++k) mma_k(d, st + 512 * (k >> 2), k, true);
+          } else {
+#pragma unroll
+            for (int k = 24; k < 36; ++k) mma_k(d, st + 512 * (k >> 2), k, true);
+          }
+        } else if (part == 0) {
+          if (half == 0) {
+#pragma unroll
+            for (int k = 16; k < 36; ++k) mma_k(d, b0 + 512 * chunk_idx(k >> 2, 0), k, k > 16);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) mma_k(d, b0 + 512 * chunk_idx(k >> 2, 1), k, k > 0);
+#pragma unroll
+            for (int k = 32; k < 36; ++k) mma_k(d, b0 + 512 * chunk_idx(k >> 2, 1), k, true);
+          }
+        } else {
+          const int v = gg % kVSlots;
+          const uint64_t vb = v == 0 ? b1 : v == 1 ? b2 : b3;
+          if (half == 0) {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) mma_k(d, vb + 512 * (k >> 2), k, true);
+          } else {
+#pragma unroll
+            for (int k = 16; k < 32; ++k) mma_k(d, vb + 512 * ((k >> 2) - 4), k, true);
+          }
         }
       };
+      // PV: B = this half's 256 latent columns (four chunks 8 KB apart), 16 keys per k-step
       auto issue_pv = [&](int gg, bool first) {
-        const uint32_t st = stage0 + (gg % kStages) * kStageBytes + 4 * half * kPageChunk;
+        uint32_t st;
+        if constexpr (kFp8) st = kOffStage + (gg % kStages) * kStageBytes + 4 * half * kPageChunk;
+        else st = kOffVPart + (gg % kVSlots) * kVPartBytes;
+        const uint64_t vd = ptx::sw128_desc(smb + st, kPageChunk, 1024);
         const uint32_t pa = tmem + 128 + (gg & 1) * 64;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint64_t db = ptx::sw128_desc(st + k * 2048, kPageChunk, 1024);
-          ptx::mma_bf16_ts(o_tm, pa + k * 8, db, kIdPV, (!first || k > 0) ? 1u : 0u);
-        }
+        for (int k = 0; k < 4; ++k)
+          ptx::mma_bf16_ts(o_tm, pa + k * 8, vd + 128 * k, kIdPV, (!first || k > 0) ? 1u : 0u);
       };
       while (ok && segs.next(seq, L, lo, hi)) {
         // Q latent 0..255: staged in the Q area by the producer, copied into TMEM columns
@@ -252,11 +390,13 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
         if (!(ok = ptx::mbar_wait(&bars.q_lo_full, nseg & 1, abort_flag, p.err))) break;
         ptx::tc_fence_after();
         // the first sequence's Q latent 0..255 was staged in the second page stage
-        const uint32_t q_stage = nseg == 0 ? stage0 + kStageBytes : qhi;
 #pragma unroll
-        for (int k = 0; k < 16; ++k)
-          ptx::tmem_cp_128x256b(tmem + k * 8, ptx::sw128_desc(q_stage + (k >> 2) * kQChunk + (k & 3) * 32, 16, 1024));
+        for (int k = 0; k < 16; ++k) {
+          const uint32_t qc = nseg == 0 ? smb + q_stage_off(k >> 2) : qhi + (k >> 2) * kQChunk;
+          ptx::tmem_cp_128x256b(tmem + k * 8, ptx::sw128_desc(qc + (k & 3) * 32, 16, 1024));
+        }
         ptx::mma_commit(&bars.q_cp_done);
+        if (nseg == 0) ptx::mma_commit(&bars.q0_copied);
         if (nseg > 0) {  // the rest of Q over the staging copy (the producer loaded the first)
           if (!(ok = ptx::mbar_wait(&bars.q_cp_done, nseg & 1, abort_flag, p.err))) break;
           ptx::mbar_arrive_expect_tx(&bars.q_hi_full, 5 * TQ * 128);
@@ -269,6 +409,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
         const int g_end = g + (hi - lo), g_first = g;
         int gs = g, gp = g;  // next page whose S / whose PV is to be issued
         int sp = 0;          // next part of S(gs)
+        bool zero_asked = false;  // bf16: the partial page gs was handed to the preparation warps
         long long t0 = clock64();
         while (gp < g_end) {
           bool progress = false;
@@ -277,15 +418,42 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
             ptx::tc_fence_after();
             issue_pv(gp, gp == g_first);
             ptx::mma_commit(&bars.o_done);
-            ptx::mma_commit(&bars.stage_empty[gp % kStages]);
+            // fp8: the whole stage; bf16: the value part (the score-only part was released
+            // after the scores)
+            ptx::mma_commit(kFp8 ? &bars.stage_empty[gp % kStages] : &bars.vpart_empty[gp % kVSlots]);
             ++gp;
             progress = true;
           }
-          // S(gs) may run at most one page ahead of the oldest unissued PV (two S buffers)
-          if (gs < g_end && gs <= gp + 1 &&
-              ptx::mbar_test_wait(&bars.stage_ready[gs % kStages][sp], (gs / kStages) & 1)) {
+          // S(gs) may run at most one page ahead of the oldest unissued PV (two S buffers).
+          // A full bf16 page needs no preparation: its parts are ready when they land.  A page
+          // that ends its sequence part-way goes to the preparation warps once both parts have
+          // landed and comes back with the rows past the end zeroed.
+          bool can = false;
+          if (gs < g_end && gs <= gp + 1) {
+            if constexpr (kFp8) {
+              can = ptx::mbar_test_wait(&bars.stage_ready[gs % kStages][sp], (gs / kStages) & 1);
+            } else if ((lo + (gs - g_first) + 1) * kPage <= L) {
+              can = sp == 0 ? ptx::mbar_test_wait(&bars.spart_full, gs & 1)
+                            : ptx::mbar_test_wait(&bars.vpart_full[gs % kVSlots], (gs / kVSlots) & 1);
+            } else if (sp == 1) {
+              can = true;  // zeroed before its part 0
+            } else if (!zero_asked) {
+              if (ptx::mbar_test_wait(&bars.spart_full, gs & 1) &&
+                  ptx::mbar_test_wait(&bars.vpart_full[gs % kVSlots], (gs / kVSlots) & 1)) {
+                ptx::mbar_arrive(&bars.zero_go);
+                zero_asked = true;
+                progress = true;
+              }
+            } else if (ptx::mbar_test_wait(&bars.zeroed, n_zeroed & 1)) {
+              can = true;
+              zero_asked = false;
+              ++n_zeroed;
+            }
+          }
+          if (can) {
             ptx::tc_fence_after();
             issue_s(gs, sp);
+            if (!kFp8 && sp == 0) ptx::mma_commit(&bars.spart_empty);
             if (sp + 1 < kParts) {
               ++sp;
             } else {
@@ -320,7 +488,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
                   : warp >= 8 ? threadIdx.x - 192
                               : kPrepOf<kFp8> + threadIdx.x - 32 * (4 + n_soft);
     const int row = tid & (kPage - 1);  // the page row whose scale (fp8) this thread stages
-    int g = 0;
+    int g = 0, n_zero = 0;
     bool ok = true;
     while (ok && segs.next(seq, L, lo, hi)) {
       for (int pg = lo; pg < hi; ++pg, ++g) {
@@ -334,21 +502,31 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
         auto live_row = [&](int rr) { return !bad && rr < valid; };
         float ksc = 0.f;
         if constexpr (kFp8) ksc = live && tid < kPage ? __ldg(p.kv_scale + (size_t)page * kPage + row) : 0.f;
-        ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.stage_full[s], (g / kStages) & 1, abort_flag, p.err));
-        if (!ok) break;
         if constexpr (!kFp8) {
+          // A page that ends its sequence part-way: once the MMA thread has seen both of its
+          // parts land it hands the page over (zero_go); rows valid..63 of its nine chunks
+          // are zeroed (16-byte granules; whole rows, so the swizzle is immaterial) and handed
+          // back (zeroed).  Full pages go straight from the copy to the MMA.
           if (valid < kPage) {
-            // zero rows valid..63 of all 9 chunks (16-byte granules)
+            ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.zero_go, n_zero & 1, abort_flag, p.err));
+            if (!ok) break;
             const int nrow = kPage - valid;
-            for (int e = tid; e < nrow * 9 * 8; e += n_prep) {
-              const int row = valid + e / 72, rem = e % 72, c = rem >> 3, gr = rem & 7;
-              *reinterpret_cast<uint4*>(st + c * kPageChunk + row * 128 + gr * 16) = make_uint4(0, 0, 0, 0);
+            for (int part = 0; part < 2; ++part) {
+              const int nch = part == 0 ? 5 : 4;
+              unsigned char* base = sm + (part == 0 ? kOffSPart : kOffVPart + (g % kVSlots) * kVPartBytes);
+              for (int e = tid; e < nrow * nch * 8; e += n_prep) {
+                const int rw = valid + e / (nch * 8), rem = e % (nch * 8), c = rem >> 3, gr = rem & 7;
+                *reinterpret_cast<uint4*>(base + c * kPageChunk + rw * 128 + gr * 16) = make_uint4(0, 0, 0, 0);
+              }
             }
+            ptx::fence_proxy_async();
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(&bars.zeroed);
+            ++n_zero;
           }
-          ptx::fence_proxy_async();
-          __syncwarp();
-          if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(&bars.stage_ready[s][0]);
         } else {
+          ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.stage_full[s], (g / kStages) & 1, abort_flag, p.err));
+          if (!ok) break;
           if (tid < kPage) bars.kscale[s][row] = ksc;
           // Widen in place, in three lockstep steps of three chunks (four 16-byte granules
           // per thread per step).  bf16 chunk c (bytes [8c, 8c+8) KB) overlaps raw chunks 2c-9
@@ -402,7 +580,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
     // -------------------------------------------------------------- softmax / epilogue
     const int r = threadIdx.x - 128;  // query row == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    int g = 0, n_epi = 0;
+    int g = 0, n_epi = 0, n_part = 0;
     bool ok = true;
     // a sequence with no cached key is in no work unit's range: unit u writes O = 0 and
     // LSE = -inf for the empty sequences u, u + G, u + 2G, ...
@@ -529,113 +707,180 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
       ptx::tc_fence_after();
       const size_t slot = (size_t)unit + seq;
       const float inv = lr > 0.f ? 1.f / lr : 0.f;
-      // partial layout [slot][column quad (128)][row (T*H)][4]: the 32 rows of a warp
-      // store one quad as 512 contiguous bytes
-      float4* dst = reinterpret_cast<float4*>(p.part_o) + (slot * 128 + half * 64) * TQ + r;
-#pragma unroll 1
-      for (int c = 0; c < 8; c += 2) {
-        uint32_t v[2][32];
-        ptx::tmem_ld32(o_addr + c * 32, v[0]);
-        ptx::tmem_ld32(o_addr + (c + 1) * 32, v[1]);
-        ptx::tmem_ld_wait();
-        if (r < TQ && gr < TH) {
-#pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2)
-#pragma unroll
-            for (int x = 0; x < 8; ++x)
-              dst[(size_t)((c + h2) * 8 + x) * TQ] =
-                  make_float4(__uint_as_float(v[h2][4 * x]) * inv, __uint_as_float(v[h2][4 * x + 1]) * inv,
-                              __uint_as_float(v[h2][4 * x + 2]) * inv, __uint_as_float(v[h2][4 * x + 3]) * inv);
-        }
-      }
-      if (r < TQ && gr < TH)
-        p.part_lse[((size_t)half * p.n_slots + slot) * TQ + r] =
-            l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-      ptx::tc_fence_before();
-      // Merge by the last split to finish: the work units that covered this virtual sequence
-      // wrote their partials of this column half into slots c + seq, c_first <= c <= c_last.
-      // Each one makes its stores visible device-wide and counts itself in; the one that
-      // completes the count (usually at the end of its unit's work) merges them:
-      // O = sum_c exp(lse_c - lse) O_c with lse = ln sum_c exp(lse_c).
-      __threadfence();
-      __syncwarp();
-      if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(&bars.part_done);
+      const float lse_own = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+      const bool row_live = r < TQ && gr < TH;
+      // The work units that cover this virtual sequence write their partials of this column
+      // half into slots c + seq, c_first <= c <= c_first + nsplit - 1; this one is k_own.
       const int n_pages = pages_of(L, kPage);
       const int c_first = segs.flat0 / bars.plan.chunk;
       const int nsplit = (segs.flat0 + n_pages - 1) / bars.plan.chunk - c_first + 1;
+      const int k_own = unit - c_first;
+      // Merge path.  A split that finds every other split of this (sequence, column half)
+      // counted in (always so for a sequence with one split) merges at once, its own share
+      // read from the accumulator.  Otherwise it writes its partial (O_half / l, LSE), makes
+      // it visible device-wide and counts itself in; the split that completes the count
+      // merges: O = sum_c exp(lse_c - lse) O_c with lse = ln sum_c exp(lse_c).
       if (r == 0) {
-        bool go = ptx::mbar_wait(&bars.part_done, n_epi & 1, abort_flag, p.err);
-        if (go) {
+        int fast = 1;
+        if (nsplit > 1) {
           // the counters were zeroed by the kernel this one was launched behind
           asm volatile("griddepcontrol.wait;" ::: "memory");
-          __threadfence();
-          const int done = atomicAdd(p.counters + (size_t)seq * 2 + half, 1) + 1;
-          __threadfence();
-          bars.merge_last = done == nsplit ? 1 : 0;
-        } else {
-          bars.merge_last = 0;
+          fast = ptx::ld_acquire_gpu(p.counters + (size_t)seq * 2 + half) == nsplit - 1;
         }
-        ptx::mbar_arrive(&bars.merge_go);
+        bars.merge_fast = fast;
+        ptx::mbar_arrive(&bars.dec_go);
       }
-      ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.merge_go, n_epi & 1, abort_flag, p.err));
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.dec_go, n_epi & 1, abort_flag, p.err));
       ++n_epi;
       if (!ok) break;
-      if (*reinterpret_cast<volatile int*>(&bars.merge_last) && r < TQ && gr < TH) {
-        // this thread's row: weights of the splits from their LSEs (read through L2, in order:
-        // they were written by other SMs during this launch)
-        const float* lsp = p.part_lse + ((size_t)half * p.n_slots + c_first + seq) * TQ + r;
-        float mxl = -INFINITY;
-        for (int k = 0; k < nsplit; ++k) mxl = fmaxf(mxl, ptx::ld_l2(lsp + (size_t)k * TQ));
-        float wsum = 0.f;
-        for (int k = 0; k < nsplit; ++k) {
-          const float ls = ptx::ld_l2(lsp + (size_t)k * TQ);
-          wsum += (mxl == -INFINITY || ls == -INFINITY) ? 0.f : __expf(ls - mxl);
+      const bool own_in_tmem = *reinterpret_cast<volatile int*>(&bars.merge_fast) != 0;
+      bool merge = own_in_tmem;
+      if (!own_in_tmem) {
+        // partial layout [slot][column quad (128)][row (T*H)][4]: the 32 rows of a warp store
+        // one quad as 512 contiguous bytes; kept in L2 ahead of the cache lines streaming past,
+        // since the merge reads it back, possibly at the end of the launch
+        const uint64_t keep = ptx::l2_policy_evict_last();
+        float4* dst = reinterpret_cast<float4*>(p.part_o) + (slot * 128 + half * 64) * TQ + r;
+#pragma unroll 1
+        for (int c = 0; c < 8; c += 2) {
+          uint32_t v[2][32];
+          ptx::tmem_ld32(o_addr + c * 32, v[0]);
+          ptx::tmem_ld32(o_addr + (c + 1) * 32, v[1]);
+          ptx::tmem_ld_wait();
+          if (row_live) {
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+              for (int x = 0; x < 8; ++x)
+                ptx::st_l2_hint(dst + (size_t)((c + h2) * 8 + x) * TQ,
+                                make_float4(__uint_as_float(v[h2][4 * x]) * inv, __uint_as_float(v[h2][4 * x + 1]) * inv,
+                                            __uint_as_float(v[h2][4 * x + 2]) * inv,
+                                            __uint_as_float(v[h2][4 * x + 3]) * inv),
+                                keep);
+          }
         }
-        const float winv = wsum > 0.f ? 1.f / wsum : 0.f;
-        auto weight = [&](int k) -> float {
-          const float ls = ptx::ld_l2(lsp + (size_t)k * TQ);
-          return (mxl == -INFINITY || ls == -INFINITY) ? 0.f : __expf(ls - mxl) * winv;
+        if (row_live) p.part_lse[((size_t)half * p.n_slots + slot) * TQ + r] = lse_own;
+        __threadfence();
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(&bars.part_done);
+        if (r == 0) {
+          bool go = ptx::mbar_wait(&bars.part_done, n_part & 1, abort_flag, p.err);
+          if (go) {
+            __threadfence();
+            const int done = atomicAdd(p.counters + (size_t)seq * 2 + half, 1) + 1;
+            __threadfence();
+            bars.merge_last = done == nsplit ? 1 : 0;
+          } else {
+            bars.merge_last = 0;
+          }
+          ptx::mbar_arrive(&bars.merge_go);
+        }
+        ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.merge_go, n_part & 1, abort_flag, p.err));
+        ++n_part;
+        if (!ok) break;
+        merge = *reinterpret_cast<volatile int*>(&bars.merge_last) != 0;
+      }
+      if (merge) {
+        // Every lane of a warp runs this block (the accumulator loads are warp-collective:
+        // a lane that skipped them would stall its warp for good); global memory is touched
+        // for the live rows only.  This thread's row: weights of the splits from their LSEs
+        // (read through L2: they were written by other SMs during this launch).
+        const float* lsp = p.part_lse + ((size_t)half * p.n_slots + c_first + seq) * TQ + r;
+        auto lse_of = [&](int k) -> float {
+          if (own_in_tmem && k == k_own) return lse_own;
+          return row_live ? ptx::ld_l2(lsp + (size_t)k * TQ) : -INFINITY;
         };
+        float mxl = -INFINITY;
+        for (int k = 0; k < nsplit; ++k) mxl = fmaxf(mxl, lse_of(k));
+        auto wraw = [&](float ls) { return (mxl == -INFINITY || ls == -INFINITY) ? 0.f : __expf(ls - mxl); };
+        float wsum = 0.f;
+        for (int k = 0; k < nsplit; ++k) wsum += wraw(lse_of(k));
+        const float winv = wsum > 0.f ? 1.f / wsum : 0.f;
+        const float w_own = own_in_tmem ? wraw(lse_own) * winv * inv : 0.f;  // on the unnormalised O
         const float4* src = reinterpret_cast<const float4*>(p.part_o) +
                             ((size_t)(c_first + seq) * 128 + half * 64) * TQ + r;
         const size_t slot_stride = (size_t)128 * TQ;
         uint4* orow = reinterpret_cast<uint4*>(
             p.out + ((size_t)(seq / p.NQT) * TH + gr) * kDl + half * 256);
-        // eight column quads of two splits per round: 16 independent 16-byte loads in flight
+        // After the unit's last segment the page stages are free (every PV product is
+        // complete and nothing more is loaded): the bf16 rows are staged there, 512 bytes per
+        // row with 16-byte chunk c of row r at chunk c ^ (r mod 32), and each warp then stores
+        // its 32 rows as one 512-byte run per instruction.  Earlier segments store straight
+        // from the row's thread.
+        bool staged;
+        {
+          Segments nx = segs;
+          int s2, L2, lo2, hi2;
+          staged = !nx.next(s2, L2, lo2, hi2);
+        }
+        unsigned char* stage_out = sm + kOffStage;
+        // sixteen column quads (64 columns) per round: 16 independent 16-byte loads of a
+        // split's partial in flight
 #pragma unroll 1
-        for (int q = 0; q < 64; q += 8) {
-          float4 acc[8];
+        for (int q = 0; q < 64; q += 16) {
+          float4 acc[16];
+          if (own_in_tmem) {
+            uint32_t v[2][32];
+            ptx::tmem_ld32(o_addr + q * 4, v[0]);
+            ptx::tmem_ld32(o_addr + q * 4 + 32, v[1]);
+            ptx::tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 8; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < 16; ++j)
+              acc[j] = make_float4(__uint_as_float(v[j >> 3][4 * (j & 7)]) * w_own,
+                                   __uint_as_float(v[j >> 3][4 * (j & 7) + 1]) * w_own,
+                                   __uint_as_float(v[j >> 3][4 * (j & 7) + 2]) * w_own,
+                                   __uint_as_float(v[j >> 3][4 * (j & 7) + 3]) * w_own);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
 #pragma unroll 1
-          for (int k = 0; k < nsplit; k += 2) {
-            const bool two = k + 1 < nsplit;
-            float4 x0[8], x1[8];
+          for (int k = 0; k < nsplit; ++k) {
+            if (own_in_tmem && k == k_own) continue;
+            float4 x[16];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              x0[j] = ptx::ld_l2(src + (size_t)k * slot_stride + (size_t)(q + j) * TQ);
-              x1[j] = two ? ptx::ld_l2(src + (size_t)(k + 1) * slot_stride + (size_t)(q + j) * TQ)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-            const float w0 = weight(k), w1 = two ? weight(k + 1) : 0.f;
+            for (int j = 0; j < 16; ++j)
+              x[j] = row_live ? ptx::ld_l2(src + (size_t)k * slot_stride + (size_t)(q + j) * TQ)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float w = wraw(lse_of(k)) * winv;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              acc[j].x += w0 * x0[j].x + w1 * x1[j].x;
-              acc[j].y += w0 * x0[j].y + w1 * x1[j].y;
-              acc[j].z += w0 * x0[j].z + w1 * x1[j].z;
-              acc[j].w += w0 * x0[j].w + w1 * x1[j].w;
+            for (int j = 0; j < 16; ++j) {
+              acc[j].x += w * x[j].x;
+              acc[j].y += w * x[j].y;
+              acc[j].z += w * x[j].z;
+              acc[j].w += w * x[j].w;
             }
           }
 #pragma unroll
-          for (int j = 0; j < 8; j += 2)
-            orow[(q + j) >> 1] = make_uint4(ptx::pack_bf16x2(acc[j].x, acc[j].y), ptx::pack_bf16x2(acc[j].z, acc[j].w),
-                                            ptx::pack_bf16x2(acc[j + 1].x, acc[j + 1].y),
-                                            ptx::pack_bf16x2(acc[j + 1].z, acc[j + 1].w));
+          for (int j = 0; j < 16; j += 2) {
+            const uint4 w = make_uint4(ptx::pack_bf16x2(acc[j].x, acc[j].y), ptx::pack_bf16x2(acc[j].z, acc[j].w),
+                                       ptx::pack_bf16x2(acc[j + 1].x, acc[j + 1].y),
+                                       ptx::pack_bf16x2(acc[j + 1].z, acc[j + 1].w));
+            const int ch = (q + j) >> 1;  // 16-byte chunk of the row's 512 bytes
+            if (staged)
+              *reinterpret_cast<uint4*>(stage_out + r * 512 + ((ch ^ (r & 31)) << 4)) = w;
+            else if (row_live)
+              orow[ch] = w;
+          }
         }
-        if (half == 0)
+        if (staged) {
+          __syncwarp();
+          const int lane = threadIdx.x & 31;
+          const int r_base = r - lane;  // the warp's 32 rows
+#pragma unroll 4
+          for (int i = 0; i < 32; ++i) {
+            const int rr = r_base + i, grr = (seq % p.NQT) * kRows + rr;
+            if (rr < TQ && grr < TH)
+              reinterpret_cast<uint4*>(p.out + ((size_t)(seq / p.NQT) * TH + grr) * kDl + half * 256)[lane] =
+                  *reinterpret_cast<const uint4*>(stage_out + rr * 512 + ((lane ^ (rr & 31)) << 4));
+          }
+        }
+        if (half == 0 && row_live)
           p.lse[((size_t)(seq / p.NQT) * p.H + gr % p.H) * p.T + gr / p.H] =
               wsum > 0.f ? mxl + logf(wsum) : -INFINITY;
       }
+      // the accumulator was read: the next segment's first PV product may overwrite it
+      ptx::tc_fence_before();
     }
   }
   ptx::tc_fence_before();
@@ -690,6 +935,21 @@ cudaError_t launch_decode_sm103(const void* q_latent, const void* q_rope, const 
       &tm, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_cache,
       dims, strides, box, /*swizzle128=*/!fp8);
   if (e != cudaSuccess) return e;
+  // The same bytes as a 3-D tensor (64 columns of a chunk, row, chunk of 64 columns): a box
+  // of 64 x 64 x n is n consecutive 64-column chunks of a page, landing chunk-major exactly as
+  // n 2-D boxes do (one TMA instruction instead of n): fp8 pages take one box of nine chunks,
+  // bf16 page parts boxes of four and five.  The chunk stride is smaller than the row stride
+  // (an overlapping view); should the driver refuse that, the 2-D boxes are used.
+  CUtensorMap tm_page = tm, tm_c4 = tm, tm_c5 = tm;
+  uint64_t pdims[3] = {64, (uint64_t)num_pages * kPage, 9};
+  uint64_t pstrides[2] = {(uint64_t)kDc * (fp8 ? 1 : 2), (uint64_t)(fp8 ? 64 : 128)};
+  const CUtensorMapDataType pdt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  auto enc3 = [&](CUtensorMap* m, uint32_t nchunks) {
+    uint32_t pbox[3] = {64, (uint32_t)kPage, nchunks};
+    return encode_tensor_map_swz(m, pdt, 3, kv_cache, pdims, pstrides, pbox, /*swizzle128=*/!fp8) == cudaSuccess;
+  };
+  const bool page_box = enc3(&tm_page, 9) && (fp8 || (enc3(&tm_c4, 4) && enc3(&tm_c5, 5)));
+  if (!page_box) tm_page = tm_c4 = tm_c5 = tm;
   // Q as 2-D tensors [B*T*H rows, 512 | 64 columns]; boxes of 64 columns x T*H rows
   // (one sequence), 128B-swizzled like the operand tiles
   const int TH = T * H;
@@ -727,6 +987,7 @@ cudaError_t launch_decode_sm103(const void* q_latent, const void* q_rope, const 
   p.causal = causal;
   p.G = G;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.page_box = page_box ? 1 : 0;
   // the split counters of the merge start at zero on every call
   const long long n_cnt = 2LL * B * p.NQT;
   if (n_cnt > 0x7fffffffLL) return cudaErrorInvalidValue;
@@ -758,7 +1019,7 @@ cudaError_t launch_decode_sm103(const void* q_latent, const void* q_rope, const 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, tm, tm_qlat, tm_qrope, p);
+    return cudaLaunchKernelEx(&cfg, kern, tm, tm_page, tm_c4, tm_c5, tm_qlat, tm_qrope, p);
   };
   return fp8 ? go(decode_split_kernel<true>) : go(decode_split_kernel<false>);
 }
