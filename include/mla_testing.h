@@ -23,6 +23,22 @@ extern "C" {
  */
 void mla_testing_decode_stall(int skip_unit, long long wait_limit_cycles);
 
+/*
+ * mla_testing_bounds_checked -- 1 when this library is the bounds-checked build (compiled
+ * with MLA_DEBUG): every store of an output, LSE or workspace element is checked against
+ * its buffer; one that falls outside is skipped and latches MLA_ERR_DEVICE_CHECK in the
+ * device error word.  0 for the normal build, which has no such checks.
+ */
+int mla_testing_bounds_checked(void);
+
+/*
+ * mla_testing_bounds_shrink -- make later launches report the output buffer `out` to the
+ * store checks as `bytes` smaller than it is (0 restores the true size), so that a test can
+ * see the bounds-checked build catch the stores of the last rows without any store leaving
+ * the real buffer.  No effect on the normal build.  Process-wide.
+ */
+void mla_testing_bounds_shrink(long long bytes);
+
 #ifdef __cplusplus
 }
 #endif

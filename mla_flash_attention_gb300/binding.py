@@ -14,10 +14,13 @@ from typing import Optional
 
 import torch
 
-_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmla_gb300.so")
+# MLA_GB300_LIB selects another build of the same library, e.g. the bounds-checked
+# libmla_gb300_debug.so (mla_flash_attention_gb300.build.build(debug=True))
+_LIB_PATH = os.environ.get("MLA_GB300_LIB") or os.path.join(
+    os.path.dirname(os.path.abspath(__file__)), "libmla_gb300.so")
 if not os.path.exists(_LIB_PATH):
     raise ImportError(
-        "libmla_gb300.so is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+        "%s is not built; run `python -c 'import __graft_entry__ as g; g.build()'`" % _LIB_PATH)
 _lib = ctypes.CDLL(_LIB_PATH)
 
 MLA_OK = 0
@@ -58,12 +61,17 @@ _lib.mla_version.restype = _i
 _lib.mla_version.argtypes = []
 _lib.mla_testing_decode_stall.restype = None
 _lib.mla_testing_decode_stall.argtypes = [_i, ctypes.c_longlong]
+_lib.mla_testing_bounds_checked.restype = _i
+_lib.mla_testing_bounds_checked.argtypes = []
+_lib.mla_testing_bounds_shrink.restype = None
+_lib.mla_testing_bounds_shrink.argtypes = [ctypes.c_longlong]
 
 EXPORTED = ("mla_prefill", "mla_decode_workspace_size", "mla_decode", "mla_decode_noalloc",
             "mla_decode_noalloc_max_workspace", "mla_cache_append", "mla_absorb",
             "mla_prefill_backward_workspace_size", "mla_prefill_backward",
             "mla_check_device_error",
-            "mla_last_error", "mla_version", "mla_testing_decode_stall")
+            "mla_last_error", "mla_version", "mla_testing_decode_stall", "mla_testing_bounds_checked",
+            "mla_testing_bounds_shrink")
 
 
 class MLAError(RuntimeError):
@@ -112,6 +120,17 @@ def testing_decode_stall(skip_unit: int = -1, wait_limit_cycles: int = 0) -> Non
     pipeline unit `skip_unit` unloaded and give each device wait `wait_limit_cycles` SM clocks.
     ``testing_decode_stall()`` restores normal calls."""
     _lib.mla_testing_decode_stall(int(skip_unit), int(wait_limit_cycles))
+
+
+def testing_bounds_checked() -> bool:
+    """True when the loaded library is the bounds-checked build (include/mla_testing.h)."""
+    return bool(_lib.mla_testing_bounds_checked())
+
+
+def testing_bounds_shrink(nbytes: int = 0) -> None:
+    """Test hook (include/mla_testing.h): later launches report `out` as `nbytes` smaller to
+    the store checks of the bounds-checked build; ``testing_bounds_shrink()`` restores them."""
+    _lib.mla_testing_bounds_shrink(int(nbytes))
 
 
 def check_device_error(stream=None) -> None:

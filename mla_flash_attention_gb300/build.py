@@ -18,6 +18,10 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmla_gb300.so")
+# the bounds-checked build (-DMLA_DEBUG): every output, LSE and workspace store is checked
+# against its buffer on the device; load it by pointing MLA_GB300_LIB at it
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_DEBUG = os.path.join(PKG, "libmla_gb300_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
@@ -38,15 +42,19 @@ def _run(cmd):
     return r.stdout + r.stderr
 
 
-def build(verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile every csrc/*.cu and link libmla_gb300.so; returns the library path."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, ptxas_info: bool = False, debug: bool = False) -> str:
+    """Compile every csrc/*.cu and link libmla_gb300.so (debug: the bounds-checked
+    libmla_gb300_debug.so); returns the library path."""
+    bdir, lib = (BUILD_DEBUG, LIB_DEBUG) if debug else (BUILD, LIB)
+    os.makedirs(bdir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    if debug:
+        extra += ["-DMLA_DEBUG"]
     nv = nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
         out = _run([nv, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj])
         return obj, out
 
@@ -57,11 +65,11 @@ def build(verbose: bool = False, ptxas_info: bool = False) -> str:
             if out.strip():
                 sys.stdout.write(out)
     objs = [o for o, _ in results]
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     _run([nv, *ARCH, "-shared", "-o", tmp, *objs])
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(verbose=True, ptxas_info="--ptxas" in sys.argv))
+    print(build(verbose=True, ptxas_info="--ptxas" in sys.argv, debug="--debug" in sys.argv))

@@ -12,11 +12,35 @@ namespace mla {
 enum : unsigned int {
   kErrTimeout = 1u,     // a bounded mbarrier / flag wait ran out
   kErrBadPage = 2u,     // a page-table entry outside [0, num_pages)
+  kErrBounds = 4u,      // a store fell outside its buffer (bounds-checked build only)
 };
 
 __device__ __forceinline__ void latch_error(unsigned int* err, unsigned int bits) {
   if (err) atomicOr(err, bits);
 }
+
+// Store bounds checks of the bounds-checked build (compiled with -DMLA_DEBUG): every store of
+// an output, LSE or workspace element goes through MLA_STORE_OK(ptr, base, bytes, err), true
+// when the element at ptr lies inside [base, base + bytes); otherwise the check latches
+// kErrBounds and the caller skips the store, so an indexing mistake shows up as an error
+// status rather than as a write outside the buffer.  In the normal build it is `true`.
+#ifdef MLA_DEBUG
+__device__ __forceinline__ bool store_ok(const void* ptr, size_t n, const void* base, size_t bytes,
+                                         unsigned int* err) {
+  const char* c = static_cast<const char*>(ptr);
+  const char* b = static_cast<const char*>(base);
+  const bool ok = c >= b && c + n <= b + bytes;
+  if (!ok) latch_error(err, kErrBounds);
+  return ok;
+}
+#define MLA_STORE_OK(ptr, base, bytes, err) ::mla::store_ok((ptr), sizeof(*(ptr)), (base), (bytes), (err))
+#else
+#define MLA_STORE_OK(ptr, base, bytes, err) true
+#endif
+
+// Bytes by which launches under-report the output buffer's size to the store checks (a test
+// hook: with a positive value the bounds-checked build must catch the last rows' stores).
+size_t testing_out_shrink();
 
 // Number of cache pages of a sequence of length L.
 __device__ __forceinline__ int pages_of(int L, int page_size) {

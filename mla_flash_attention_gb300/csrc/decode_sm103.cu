@@ -95,6 +95,8 @@ struct Params {
   int n_slots;  // partial slots: G + B * NQT
   float scale_log2;
   int page_box;  // 1: a page is one box of the 3-D cache map (else nine boxes of the 2-D one)
+  // buffer sizes for the store checks of the bounds-checked build
+  size_t out_bytes, lse_bytes, part_o_bytes, part_lse_bytes, counters_bytes;
 };
 
 struct Bars {
@@ -588,8 +590,12 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
       for (int b = unit; b < p.B; b += p.G) {
         if (clamp_len(__ldg(p.cache_lens + b), p.max_pages) > 0) continue;
         uint4* o = reinterpret_cast<uint4*>(p.out + (size_t)b * TH * kDl);
-        for (int i = r; i < TH * (kDl / 8); i += 32 * n_soft) o[i] = make_uint4(0, 0, 0, 0);
-        for (int i = r; i < TH; i += 32 * n_soft) p.lse[((size_t)b * p.H + i % p.H) * p.T + i / p.H] = -INFINITY;
+        for (int i = r; i < TH * (kDl / 8); i += 32 * n_soft)
+          if (MLA_STORE_OK(o + i, p.out, p.out_bytes, p.err)) o[i] = make_uint4(0, 0, 0, 0);
+        for (int i = r; i < TH; i += 32 * n_soft) {
+          float* lp = p.lse + ((size_t)b * p.H + i % p.H) * p.T + i / p.H;
+          if (MLA_STORE_OK(lp, p.lse, p.lse_bytes, p.err)) *lp = -INFINITY;
+        }
       }
     }
     while (ok && segs.next(seq, L, lo, hi)) {
@@ -751,15 +757,19 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
-              for (int x = 0; x < 8; ++x)
-                ptx::st_l2_hint(dst + (size_t)((c + h2) * 8 + x) * TQ,
-                                make_float4(__uint_as_float(v[h2][4 * x]) * inv, __uint_as_float(v[h2][4 * x + 1]) * inv,
-                                            __uint_as_float(v[h2][4 * x + 2]) * inv,
-                                            __uint_as_float(v[h2][4 * x + 3]) * inv),
-                                keep);
+              for (int x = 0; x < 8; ++x) {
+                float4* d4 = dst + (size_t)((c + h2) * 8 + x) * TQ;
+                if (MLA_STORE_OK(d4, p.part_o, p.part_o_bytes, p.err))
+                  ptx::st_l2_hint(d4,
+                                  make_float4(__uint_as_float(v[h2][4 * x]) * inv, __uint_as_float(v[h2][4 * x + 1]) * inv,
+                                              __uint_as_float(v[h2][4 * x + 2]) * inv,
+                                              __uint_as_float(v[h2][4 * x + 3]) * inv),
+                                  keep);
+              }
           }
         }
-        if (row_live) p.part_lse[((size_t)half * p.n_slots + slot) * TQ + r] = lse_own;
+        float* plp = p.part_lse + ((size_t)half * p.n_slots + slot) * TQ + r;
+        if (row_live && MLA_STORE_OK(plp, p.part_lse, p.part_lse_bytes, p.err)) *plp = lse_own;
         __threadfence();
         __syncwarp();
         if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(&bars.part_done);
@@ -767,7 +777,8 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
           bool go = ptx::mbar_wait(&bars.part_done, n_part & 1, abort_flag, p.err);
           if (go) {
             __threadfence();
-            const int done = atomicAdd(p.counters + (size_t)seq * 2 + half, 1) + 1;
+            int* cnt = p.counters + (size_t)seq * 2 + half;
+            const int done = MLA_STORE_OK(cnt, p.counters, p.counters_bytes, p.err) ? atomicAdd(cnt, 1) + 1 : 0;
             __threadfence();
             bars.merge_last = done == nsplit ? 1 : 0;
           } else {
@@ -859,7 +870,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
             const int ch = (q + j) >> 1;  // 16-byte chunk of the row's 512 bytes
             if (staged)
               *reinterpret_cast<uint4*>(stage_out + r * 512 + ((ch ^ (r & 31)) << 4)) = w;
-            else if (row_live)
+            else if (row_live && MLA_STORE_OK(orow + ch, p.out, p.out_bytes, p.err))
               orow[ch] = w;
           }
         }
@@ -870,14 +881,14 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
 #pragma unroll 4
           for (int i = 0; i < 32; ++i) {
             const int rr = r_base + i, grr = (seq % p.NQT) * kRows + rr;
-            if (rr < TQ && grr < TH)
-              reinterpret_cast<uint4*>(p.out + ((size_t)(seq / p.NQT) * TH + grr) * kDl + half * 256)[lane] =
-                  *reinterpret_cast<const uint4*>(stage_out + rr * 512 + ((lane ^ (rr & 31)) << 4));
+            uint4* od = reinterpret_cast<uint4*>(p.out + ((size_t)(seq / p.NQT) * TH + grr) * kDl + half * 256) + lane;
+            if (rr < TQ && grr < TH && MLA_STORE_OK(od, p.out, p.out_bytes, p.err))
+              *od = *reinterpret_cast<const uint4*>(stage_out + rr * 512 + ((lane ^ (rr & 31)) << 4));
           }
         }
-        if (half == 0 && row_live)
-          p.lse[((size_t)(seq / p.NQT) * p.H + gr % p.H) * p.T + gr / p.H] =
-              wsum > 0.f ? mxl + logf(wsum) : -INFINITY;
+        float* lp = p.lse + ((size_t)(seq / p.NQT) * p.H + gr % p.H) * p.T + gr / p.H;
+        if (half == 0 && row_live && MLA_STORE_OK(lp, p.lse, p.lse_bytes, p.err))
+          *lp = wsum > 0.f ? mxl + logf(wsum) : -INFINITY;
       }
       // the accumulator was read: the next segment's first PV product may overwrite it
       ptx::tc_fence_before();
@@ -988,6 +999,12 @@ cudaError_t launch_decode_sm103(const void* q_latent, const void* q_rope, const 
   p.G = G;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   p.page_box = page_box ? 1 : 0;
+  const size_t out_full = (size_t)B * T * H * kDl * 2;
+  p.out_bytes = out_full - std::min(out_full, testing_out_shrink());
+  p.lse_bytes = (size_t)B * H * T * sizeof(float);
+  p.part_o_bytes = (size_t)(reinterpret_cast<char*>(part_lse) - reinterpret_cast<char*>(part_o));
+  p.part_lse_bytes = (size_t)(reinterpret_cast<char*>(counters) - reinterpret_cast<char*>(part_lse));
+  p.counters_bytes = (size_t)2 * B * p.NQT * sizeof(int);
   // the split counters of the merge start at zero on every call
   const long long n_cnt = 2LL * B * p.NQT;
   if (n_cnt > 0x7fffffffLL) return cudaErrorInvalidValue;

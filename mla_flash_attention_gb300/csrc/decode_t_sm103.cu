@@ -100,6 +100,8 @@ struct Params {
   float scale_log2;
   long long wait_limit;  // SM clocks a pipeline wait may last before it gives up
   int skip_unit;         // test hook: >= 0 leaves that raw unit unloaded (a wait then runs out)
+  // buffer sizes for the store checks of the bounds-checked build
+  size_t out_bytes, lse_bytes, part_o_bytes, part_lse_bytes, counters_bytes;
 };
 
 struct Bars {
@@ -620,8 +622,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = unit; b < p.B; b += p.G) {
       if (clamp_len(__ldg(p.cache_lens + b), p.max_pages) > 0) continue;
       uint4* o = reinterpret_cast<uint4*>(p.out + (size_t)b * TH * kDl);
-      for (int i = st; i < TH * (kDl / 8); i += 128) o[i] = make_uint4(0, 0, 0, 0);
-      for (int i = st; i < TH; i += 128) p.lse[((size_t)b * p.H + i % p.H) * p.T + i / p.H] = -INFINITY;
+      for (int i = st; i < TH * (kDl / 8); i += 128)
+        if (MLA_STORE_OK(o + i, p.out, p.out_bytes, p.err)) o[i] = make_uint4(0, 0, 0, 0);
+      for (int i = st; i < TH; i += 128) {
+        float* lp = p.lse + ((size_t)b * p.H + i % p.H) * p.T + i / p.H;
+        if (MLA_STORE_OK(lp, p.lse, p.lse_bytes, p.err)) *lp = -INFINITY;
+      }
     }
     // key scales one block ahead (the iterator already holds the next block and its pages)
     auto fetch_ks = [&](const Block& bb) -> float {
@@ -822,12 +828,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t)cur.seq * TH * kDl + col;
 #pragma unroll
           for (int q = 0; q < NP; ++q)
-            if (q < TQ) o[(size_t)q * kDl] = __float2bfloat16_rn(__uint_as_float(ov[q]) * inv[q]);
+            if (q < TQ && MLA_STORE_OK(o + (size_t)q * kDl, p.out, p.out_bytes, p.err))
+              o[(size_t)q * kDl] = __float2bfloat16_rn(__uint_as_float(ov[q]) * inv[q]);
         } else {
           float* o = p.part_o + slot * TQ * kDl + col;
 #pragma unroll
           for (int q = 0; q < NP; ++q)
-            if (q < TQ) o[(size_t)q * kDl] = __uint_as_float(ov[q]) * inv[q];
+            if (q < TQ && MLA_STORE_OK(o + (size_t)q * kDl, p.part_o, p.part_o_bytes, p.err))
+              o[(size_t)q * kDl] = __uint_as_float(ov[q]) * inv[q];
         }
       }
       ptx::tc_fence_before();
@@ -839,10 +847,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < NP; ++q) mq = q == st ? m[q] : mq;
         const float l = bars.colv[st];
         const float ls = l > 0.f ? (mq + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-        if (whole)
-          p.lse[((size_t)cur.seq * p.H + st % p.H) * p.T + st / p.H] = ls;
-        else
-          p.part_lse[slot * TQ + st] = ls;
+        float* lp = p.lse + ((size_t)cur.seq * p.H + st % p.H) * p.T + st / p.H;
+        float* plp = p.part_lse + slot * TQ + st;
+        if (whole) {
+          if (MLA_STORE_OK(lp, p.lse, p.lse_bytes, p.err)) *lp = ls;
+        } else if (MLA_STORE_OK(plp, p.part_lse, p.part_lse_bytes, p.err)) {
+          *plp = ls;
+        }
       }
       if (whole) continue;
       // Merge by the last split to finish: the units that covered this sequence wrote their
@@ -855,7 +866,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (st == 0) {
         asm volatile("griddepcontrol.wait;" ::: "memory");  // counters zeroed by the kernel ahead
         __threadfence();
-        const int done = atomicAdd(p.counters + cur.seq, 1) + 1;
+        int* cnt = p.counters + cur.seq;
+        const int done = MLA_STORE_OK(cnt, p.counters, p.counters_bytes, p.err) ? atomicAdd(cnt, 1) + 1 : 0;
         __threadfence();
         bars.merge_last = done == nsplit ? 1 : 0;
       }
@@ -875,7 +887,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         bars.mx[st] = mx;
         bars.winv[st] = ws > 0.f ? 1.f / ws : 0.f;
-        p.lse[((size_t)cur.seq * p.H + st % p.H) * p.T + st / p.H] = ws > 0.f ? mx + logf(ws) : -INFINITY;
+        float* lp = p.lse + ((size_t)cur.seq * p.H + st % p.H) * p.T + st / p.H;
+        if (MLA_STORE_OK(lp, p.lse, p.lse_bytes, p.err)) *lp = ws > 0.f ? mx + logf(ws) : -INFINITY;
       }
       if (!(ok = group_sync())) break;
       // thread st: latent quad st (columns 4 st .. 4 st + 3) of every row, four rows and two
@@ -914,10 +927,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          if (q0 + i < TQ)
-            *reinterpret_cast<uint2*>(p.out + ((size_t)cur.seq * TH + q0 + i) * kDl + 4 * st) =
-                make_uint2(ptx::pack_bf16x2(acc[i].x, acc[i].y), ptx::pack_bf16x2(acc[i].z, acc[i].w));
+        for (int i = 0; i < 4; ++i) {
+          uint2* od = reinterpret_cast<uint2*>(p.out + ((size_t)cur.seq * TH + q0 + i) * kDl + 4 * st);
+          if (q0 + i < TQ && MLA_STORE_OK(od, p.out, p.out_bytes, p.err))
+            *od = make_uint2(ptx::pack_bf16x2(acc[i].x, acc[i].y), ptx::pack_bf16x2(acc[i].z, acc[i].w));
+        }
       }
     }
   }
@@ -1003,6 +1017,12 @@ cudaError_t launch_decode_t_sm103(const void* q_latent, const void* q_rope, cons
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   p.wait_limit = wait_limit;
   p.skip_unit = skip_unit;
+  const size_t out_full = (size_t)B * T * H * kDl * 2;
+  p.out_bytes = out_full - std::min(out_full, testing_out_shrink());
+  p.lse_bytes = (size_t)B * H * T * sizeof(float);
+  p.part_o_bytes = (size_t)(reinterpret_cast<char*>(part_lse) - reinterpret_cast<char*>(part_o));
+  p.part_lse_bytes = (size_t)(reinterpret_cast<char*>(counters) - reinterpret_cast<char*>(part_lse));
+  p.counters_bytes = (size_t)B * sizeof(int);
   const int zero_blocks = std::min((B + 2047) / 2048, 1024);
   zero_counters_t_kernel<<<zero_blocks, 256, 0, stream>>>(counters, B);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;

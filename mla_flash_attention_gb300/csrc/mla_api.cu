@@ -111,6 +111,9 @@ bool decode_transposed(bool fp8, int TH) { return fp8 && TH <= kTransposedMaxRow
 // `g_skip_unit` unloaded and gives each pipeline wait `g_wait_limit` SM clocks.
 std::atomic<int> g_skip_unit{-1};
 std::atomic<long long> g_wait_limit{1000000000LL};
+// ... and launches report the output buffer `g_out_shrink` bytes smaller to the store checks
+// of the bounds-checked build
+std::atomic<size_t> g_out_shrink{0};
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -157,6 +160,8 @@ DecodeWorkspace decode_workspace_layout_t(void* base, int B, int TH, int d_laten
 }  // namespace
 
 namespace mla {
+size_t testing_out_shrink() { return g_out_shrink.load(); }
+
 // The device error word's address on the current device (for entry points in other files).
 unsigned int* error_word_address() { return device_error_word(); }
 
@@ -181,6 +186,16 @@ void mla_testing_decode_stall(int skip_unit, long long wait_limit_cycles) {
   g_wait_limit.store(wait_limit_cycles > 0 ? wait_limit_cycles : 1000000000LL);
 }
 
+void mla_testing_bounds_shrink(long long bytes) { g_out_shrink.store(bytes > 0 ? (size_t)bytes : 0); }
+
+int mla_testing_bounds_checked(void) {
+#ifdef MLA_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
+}
+
 int mla_version(void) { return 100; }
 
 mla_status mla_check_device_error(void* stream) {
@@ -197,6 +212,8 @@ mla_status mla_check_device_error(void* stream) {
   if (v & mla::kErrTimeout) return fail(MLA_ERR_TIMEOUT, "a device-side pipeline wait timed out (word 0x%x)", v);
   if (v & mla::kErrBadPage)
     return fail(MLA_ERR_DEVICE_CHECK, "a page-table entry or cache length was out of range (word 0x%x)", v);
+  if (v & mla::kErrBounds)
+    return fail(MLA_ERR_DEVICE_CHECK, "a store fell outside its buffer and was skipped (word 0x%x)", v);
   return MLA_OK;
 }
 

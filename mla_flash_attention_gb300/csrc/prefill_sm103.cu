@@ -48,6 +48,7 @@ struct Params {
   void* out;
   float* lse;
   unsigned int* err;
+  size_t out_bytes, lse_bytes;  // for the store checks of the bounds-checked build
 };
 
 struct Bars {
@@ -353,7 +354,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + row_off + c * 32);
 #pragma unroll
             for (int x = 0; x < 8; ++x)
-              dst[x] = make_float4(__uint_as_float(v[4 * x]) * inv, __uint_as_float(v[4 * x + 1]) * inv,
+              if (MLA_STORE_OK(dst + x, p.out, p.out_bytes, p.err))
+                dst[x] = make_float4(__uint_as_float(v[4 * x]) * inv, __uint_as_float(v[4 * x + 1]) * inv,
                                    __uint_as_float(v[4 * x + 2]) * inv, __uint_as_float(v[4 * x + 3]) * inv);
           } else {
             uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + row_off + c * 32);
@@ -364,13 +366,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               w.y = ptx::pack_bf16x2(__uint_as_float(v[8 * x + 2]) * inv, __uint_as_float(v[8 * x + 3]) * inv);
               w.z = ptx::pack_bf16x2(__uint_as_float(v[8 * x + 4]) * inv, __uint_as_float(v[8 * x + 5]) * inv);
               w.w = ptx::pack_bf16x2(__uint_as_float(v[8 * x + 6]) * inv, __uint_as_float(v[8 * x + 7]) * inv);
-              dst[x] = w;
+              if (MLA_STORE_OK(dst + x, p.out, p.out_bytes, p.err)) dst[x] = w;
             }
           }
         }
       }
       if (store)
-        p.lse[(static_cast<size_t>(b) * p.H + h) * p.S + i] =
+        if (MLA_STORE_OK(p.lse + (static_cast<size_t>(b) * p.H + h) * p.S + i, p.lse, p.lse_bytes, p.err))
+          p.lse[(static_cast<size_t>(b) * p.H + h) * p.S + i] =
             l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
     }
   }
@@ -425,6 +428,11 @@ cudaError_t launch_prefill_sm103_bf16(const void* q_nope, const void* q_rope, co
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   p.out = out;
   p.lse = lse;
+  {
+    const size_t out_full = (size_t)B * S * H * 128 * (out_f32 ? 4 : 2);
+    p.out_bytes = out_full - (testing_out_shrink() < out_full ? testing_out_shrink() : out_full);
+    p.lse_bytes = (size_t)B * H * S * sizeof(float);
+  }
   p.err = err;
   // The warpgroups trade registers at run time (setmaxnreg): the producer/MMA warpgroup drops
   // to kRegsLow and the two softmax warpgroups rise to kRegsHigh.  The raised counts are drawn

@@ -176,3 +176,9 @@ def test_cache_append_argument_checks(clib):
     assert call(dt=1, scale=18) == 1  # scales not 4-byte aligned
     assert call(cache=40) == 1       # misaligned
     assert call(dt=5) == 2
+
+
+def test_normal_build_has_no_bounds_checks(clib):
+    # the device-side store checks exist only in the bounds-checked build (MLA_DEBUG)
+    clib.mla_testing_bounds_checked.restype = ctypes.c_int
+    assert clib.mla_testing_bounds_checked() == 0
