@@ -691,15 +691,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         qs[q + 2] = v.z;
         qs[q + 3] = v.w;
       }
-      bool grow = false;
+      // Row q is (token q / H, head q % H) and sees the key iff key <= L - T + q / H (causal),
+      // i.e. iff q >= H (key - (L - T)): the rows that see this key are q_lo .. TQ - 1, found
+      // with one multiply (no division or branch in the loop below)
+      int q_lo = 0;
+      if (key > vis_all) q_lo = p.causal ? p.H * (key - (cur.L - p.T)) : NP;
+      if (!valid) q_lo = NP;
+      // (the first block of a segment always sets the references; the old ones are stale)
+      bool grow = cur.first;
 #pragma unroll
       for (int q = 0; q < NP; ++q) {
-        bool see = valid && q < TQ;
-        if (key > vis_all) see = see && p.causal && key <= cur.L - p.T + q / p.H;
+        const bool see = q >= q_lo && q < TQ;
         const float x = see ? fmaf(u[q], qs[q] * ks, lks) : -INFINITY;
         u[q] = x;
-        // (the first block of a segment always sets the references; the old ones are stale)
-        grow = grow || cur.first || (x > m[q] + kTau);
+        grow |= x > m[q] + kTau;
       }
       // does any key of the block exceed its row's reference by more than 2^kTau?
       const unsigned wv = __ballot_sync(0xffffffffu, grow);
