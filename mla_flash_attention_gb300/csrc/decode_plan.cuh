@@ -1,12 +1,15 @@
 // Split plan of the decode key axis, shared by the decode kernels.
 //
 // The pages of all (sequence, query tile) work items are numbered in order (item v owns flat
-// pages [P_v, P_v + n_v)), and work unit c of G takes flat pages [c*chunk, (c+1)*chunk) with
-// chunk = ceil(total / G).  Every CTA computes its unit's plan from cache_lens alone.  The
+// pages [P_v, P_v + n_v + item_cost)), and work unit c of G takes flat pages
+// [c*chunk, (c+1)*chunk) with chunk = ceil(total / G).  The item_cost flat pages after a
+// non-empty item's n_v pages hold no keys: a unit pays for every item it touches (loading the
+// item's queries, its epilogue and partial, the merge), so units that touch more items get
+// fewer real pages.  Every CTA computes its unit's plan from cache_lens alone.  The
 // partial result of unit c for item v goes to slot c + v, which is unique because consecutive
 // units never move backwards through the items; there are at most G + (items) - 1 slots.
 // A parameter struct passed to make_plan / Segments::init provides cache_lens, B, NQT
-// (query tiles per sequence), max_pages and G.
+// (query tiles per sequence), max_pages, G and item_cost (flat pages charged per item).
 #pragma once
 
 #include "common.cuh"
@@ -39,7 +42,8 @@ __device__ void make_plan(const Prm& prm, int unit, Plan* out) {
   const int lane = threadIdx.x & 31;
   const int B = prm.B * prm.NQT;  // work is planned per (sequence, query tile)
   auto pages_at = [&](int bb) {
-    return bb < B ? pages_of(clamp_len(__ldg(prm.cache_lens + bb / prm.NQT), prm.max_pages), kPage) : 0;
+    const int n = bb < B ? pages_of(clamp_len(__ldg(prm.cache_lens + bb / prm.NQT), prm.max_pages), kPage) : 0;
+    return n > 0 ? n + prm.item_cost : 0;
   };
   int total = 0;
   for (int base = 0; base < B; base += 256) {
@@ -87,13 +91,14 @@ __device__ void make_plan(const Prm& prm, int unit, Plan* out) {
 // role runs its own copy and sees the same sequence.
 struct Segments {
   const int* lens;
-  int B, NQT, max_pages, start, end, b, pb;
+  int B, NQT, max_pages, item_cost, start, end, b, pb;
   template <typename Prm>
   __device__ void init(const Prm& prm, const Plan& plan) {
     lens = prm.cache_lens;
     NQT = prm.NQT;
     B = prm.B * prm.NQT;
     max_pages = prm.max_pages;
+    item_cost = prm.item_cost;
     start = plan.start;
     end = plan.end;
     b = plan.b0;
@@ -101,6 +106,7 @@ struct Segments {
   }
   // Next non-empty segment: sets seq (the virtual sequence: sequence * NQT + query tile),
   // L, lo, hi (page indices within the sequence); flat0 = the sequence's first flat page.
+  // A unit whose range reaches only into an item's key-less flat pages gets no segment of it.
   // Lengths are fetched eight at a time so that skipping to this unit's first sequence
   // costs one load latency per eight sequences rather than one per sequence.
   int flat0 = 0;
@@ -114,9 +120,10 @@ struct Segments {
         if (b >= B || pb >= end) return false;
         const int Lb = clamp_len(Ls[i], max_pages);
         const int n = pages_of(Lb, kPage);
-        const int l0 = max(start, pb) - pb, h0 = min(end, pb + n) - pb;
+        const int nv = n > 0 ? n + item_cost : 0;  // flat pages of the item
+        const int l0 = max(start, pb) - pb, h0 = min(min(end, pb + nv) - pb, n);
         const int cur = b, cur_pb = pb;
-        pb += n;
+        pb += nv;
         ++b;
         if (l0 < h0) {
           flat0 = cur_pb;

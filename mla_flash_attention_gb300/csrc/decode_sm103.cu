@@ -95,6 +95,7 @@ struct Params {
   int n_slots;  // partial slots: G + B * NQT
   float scale_log2;
   int page_box;  // 1: a page is one box of the 3-D cache map (else nine boxes of the 2-D one)
+  int item_cost;  // flat pages the split plan charges per work item (see decode_plan.cuh)
   // buffer sizes for the store checks of the bounds-checked build
   size_t out_bytes, lse_bytes, part_o_bytes, part_lse_bytes, counters_bytes;
 };
@@ -999,6 +1000,9 @@ cudaError_t launch_decode_sm103(const void* q_latent, const void* q_rope, const 
   p.G = G;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   p.page_box = page_box ? 1 : 0;
+  // no charge per work item: an item costs this kernel about a page (its Q load overlaps the
+  // previous item's pages), and the even split measured best
+  p.item_cost = 0;
   const size_t out_full = (size_t)B * T * H * kDl * 2;
   p.out_bytes = out_full - std::min(out_full, testing_out_shrink());
   p.lse_bytes = (size_t)B * H * T * sizeof(float);

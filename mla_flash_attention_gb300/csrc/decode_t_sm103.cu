@@ -100,6 +100,7 @@ struct Params {
   float scale_log2;
   long long wait_limit;  // SM clocks a pipeline wait may last before it gives up
   int skip_unit;         // test hook: >= 0 leaves that raw unit unloaded (a wait then runs out)
+  int item_cost;         // flat pages the split plan charges per work item (see decode_plan.cuh)
   // buffer sizes for the store checks of the bounds-checked build
   size_t out_bytes, lse_bytes, part_o_bytes, part_lse_bytes, counters_bytes;
 };
@@ -1022,6 +1023,8 @@ cudaError_t launch_decode_t_sm103(const void* q_latent, const void* q_rope, cons
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   p.wait_limit = wait_limit;
   p.skip_unit = skip_unit;
+  // an item (its Q preparation, epilogue and merge) costs this kernel about three pages
+  p.item_cost = 3;
   const size_t out_full = (size_t)B * T * H * kDl * 2;
   p.out_bytes = out_full - std::min(out_full, testing_out_shrink());
   p.lse_bytes = (size_t)B * H * T * sizeof(float);
