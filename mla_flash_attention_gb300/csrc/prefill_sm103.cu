@@ -153,6 +153,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tma_load_4d(dst, &tm_v, &bars.ring_full[s], 0, h, key0, b);
           ptx::tma_load_4d(dst + kChunk, &tm_v, &bars.ring_full[s], 64, h, key0, b);
         }
+        // warm L2 with the key tile two ahead: its ring slot frees only once this tile's PV is
+        // done, and the load then pays the full latency unless the bytes are already in L2
+        if (j + 2 < n_kv) {
+          const int key2 = key0 + 2 * BN;
+          ptx::tma_prefetch_4d(&tm_kn, 0, h, key2, b);
+          ptx::tma_prefetch_4d(&tm_kn, 64, h, key2, b);
+          ptx::tma_prefetch_3d(&tm_kr, 0, key2, b);
+          ptx::tma_prefetch_4d(&tm_v, 0, h, key2, b);
+          ptx::tma_prefetch_4d(&tm_v, 64, h, key2, b);
+        }
       }
     } else if (warp == 1 && ptx::elect_one()) {
       // ------------------------------------------------------------ MMA issuer
