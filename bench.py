@@ -118,7 +118,12 @@ def recorded_traffic(key, src_files):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 20 ms while running."""
+    """nvidia-smi clocks and throttle reasons sampled every 20 ms while running.
+
+    Starting nvidia-smi perturbs the GPU for a while (measured: the headline prefill 2 %
+    slower when the sampler starts with its timed loop), so `ready()` waits for the first
+    sample before the caller times anything, and `mark()` makes the summary count only the
+    samples taken after it (the timed region)."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -127,7 +132,27 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.idx = gpu_index
         self.proc = None
+        self.first = 0
         self.path = os.path.join("/tmp", "mla_clocks_%d_%d.csv" % (os.getpid(), gpu_index))
+
+    def _lines(self):
+        try:
+            with open(self.path) as fh:
+                return sum(1 for _ in fh)
+        except OSError:
+            return 0
+
+    def ready(self, timeout_s=5.0):
+        """Wait (up to timeout_s) until nvidia-smi has written its first sample."""
+        t0 = time.time()
+        while self.proc is not None and self._lines() == 0 and time.time() - t0 < timeout_s:
+            time.sleep(0.05)
+        return self
+
+    def mark(self):
+        """Count only the samples written from now on."""
+        self.first = self._lines()
+        return self
 
     def __enter__(self):
         try:
@@ -153,7 +178,9 @@ class ClockSampler:
             return None
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
+        for k, line in enumerate(open(self.path)):
+            if k < self.first:
+                continue
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
@@ -302,7 +329,12 @@ def run_gpu(args):
 
     barrier()
     with ClockSampler(local) as clk:
-        ms = time_calls(call_prefill, args.steps, args.warmup)
+        clk.ready()
+        for _ in range(args.warmup):
+            call_prefill()
+        torch.cuda.synchronize()
+        clk.mark()
+        ms = time_calls(call_prefill, args.steps, 0)
     barrier()
     ms_mean = max_over_ranks(sum(ms) / len(ms))
     clocks = clk.summary()
