@@ -82,6 +82,7 @@ struct Params {
   const uint16_t* q_latent;  // [B, T, H, 512]
   const uint16_t* q_rope;    // [B, T, H, 64]
   const float* kv_scale;     // [num_pages, 64] (fp8 path)
+  const unsigned char* cache_bytes;  // the cache as bytes: page g at g * 64 * 576 * element size
   const int* page_table;
   const int* cache_lens;
   float* part_o;
@@ -115,17 +116,23 @@ struct Bars {
   uint64_t q0_copied;  // the first sequence's staged Q is in TMEM (one phase per launch)
   uint64_t part_done, merge_go;  // partial written by the 4 softmax warps / merge decision
   uint64_t dec_go;               // the segment's merge path decided
-  int merge_last, merge_fast;
+  uint64_t merge_full;           // the other split's partial copied into shared memory
+  int merge_last, merge_fast, merge_bulk;
   uint32_t tmem_base;
   int abort_flag;
   Plan plan;
   float kscale[kStages][kPage];
 };
 
-__device__ __forceinline__ int page_row(const Params& p, int vseq, int pg) {
-  const int page = __ldg(p.page_table + (size_t)(vseq / p.NQT) * p.max_pages + pg);
+__device__ __forceinline__ int page_of(const Params& p, int vseq, int pg) {
+  return __ldg(p.page_table + (size_t)(vseq / p.NQT) * p.max_pages + pg);
+}
+__device__ __forceinline__ int row_of_page(const Params& p, int page) {
   // an out-of-range page reads as zeros (coordinates outside the tensor) and is masked
   return (page >= 0 && page < p.num_pages) ? page * kPage : -2 * kPage;
+}
+__device__ __forceinline__ int page_row(const Params& p, int vseq, int pg) {
+  return row_of_page(p, page_of(p, vseq, pg));
 }
 
 template <bool kFp8>
@@ -162,6 +169,16 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
   auto q_row0 = [&](int v) { return (v / p.NQT) * TH + (v % p.NQT) * kRows; };
 
   if (threadIdx.x == 0) {
+    // the descriptors are fetched while the barriers are set up and the plan is made: a TMA
+    // instruction whose map is not cached waits for that fetch
+    ptx::prefetch_tensormap(&tm_qlat);
+    ptx::prefetch_tensormap(&tm_qrope);
+    if (kFp8 || p.page_box) ptx::prefetch_tensormap(&tm_page);
+    if (!kFp8 && p.page_box) {
+      ptx::prefetch_tensormap(&tm_c4);
+      ptx::prefetch_tensormap(&tm_c5);
+    }
+    ptx::prefetch_tensormap(&tm_cache);
     bars.abort_flag = 0;
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&bars.stage_full[s], 1);
@@ -191,14 +208,16 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
     ptx::mbar_init(&bars.part_done, n_soft);
     ptx::mbar_init(&bars.merge_go, 1);
     ptx::mbar_init(&bars.dec_go, 1);
+    ptx::mbar_init(&bars.merge_full, 1);
     ptx::fence_barrier_init();
   }
+  // the plan's length loads go out first; the other warps set up meanwhile
+  if (warp == 3) make_plan(p, unit, &bars.plan);
   // Q rows T*H..127 are never loaded: keep them zero (finite scores in the padded rows)
   for (int i = threadIdx.x; i < 5 * kQChunk / 16; i += kThreads)
     reinterpret_cast<uint4*>(sm + kOffQhi)[i] = make_uint4(0, 0, 0, 0);
   ptx::fence_proxy_async();
   if (warp == 2) ptx::tmem_alloc(&bars.tmem_base, 512);
-  if (warp == 3) make_plan(p, unit, &bars.plan);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -214,11 +233,12 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
     // the value part, which is released later) and the L2 warming.  Copies are served in
     // issue order, so a page's value part never waits behind the next page's score-only part.
     if ((threadIdx.x & 31) == 0) {
-      ptx::prefetch_tensormap(&tm_cache);
-      ptx::prefetch_tensormap(&tm_qlat);
       int g = 0, nseg = 0;
       bool ok = true;
       while (ok && segs.next(seq, L, lo, hi)) {
+        // the first page's table entry is read before Q is issued, so its latency overlaps
+        // the Q copies instead of delaying the page's own
+        const int page_first = page_of(p, seq, lo);
         {
           if (nseg == 0) {
             // first sequence: Q latent 0..255 staged in the (still unused) second page
@@ -238,18 +258,20 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
               ptx::tma_load_2d(sm + kOffQhi + c * kQChunk, &tm_qlat, &bars.q_lo_full, c * 64, q_row0(seq));
           }
           ++nseg;
-          {  // warm L2 with the next segment's Q, read when this one's pages are done
-            Segments nx = segs;
-            int s2, L2, lo2, hi2;
-            if (nx.next(s2, L2, lo2, hi2)) {
-              const int r0 = q_row0(s2), rows = min(TQ, p.B * TH - r0);
-              if (rows > 0) {
-                ptx::bulk_prefetch(p.q_latent + (size_t)r0 * kDl, rows * kDl * 2);
-                ptx::bulk_prefetch(p.q_rope + (size_t)r0 * 64, rows * 128);
-              }
+        }
+        // warm L2 with the next segment's Q (read when this one's pages are done) once this
+        // segment's first page is issued: finding the next segment reads the lengths again
+        auto warm_next_q = [&]() {
+          Segments nx = segs;
+          int s2, L2, lo2, hi2;
+          if (nx.next(s2, L2, lo2, hi2)) {
+            const int r0 = q_row0(s2), rows = min(TQ, p.B * TH - r0);
+            if (rows > 0) {
+              ptx::bulk_prefetch(p.q_latent + (size_t)r0 * kDl, rows * kDl * 2);
+              ptx::bulk_prefetch(p.q_rope + (size_t)r0 * 64, rows * 128);
             }
           }
-        }
+        };
         for (int pg = lo; pg < hi; ++pg, ++g) {
           const int s = g % kStages;
           if (!(ok = ptx::mbar_wait(kFp8 ? &bars.stage_empty[s] : &bars.spart_empty,
@@ -257,7 +279,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
             break;
           // the first sequence's staged Q stays in place until it is copied to TMEM
           if (kFp8 && g == 1 && !(ok = ptx::mbar_wait(&bars.q0_copied, 0, abort_flag, p.err))) break;
-          const int y = page_row(p, seq, pg);
+          const int y = pg == lo ? row_of_page(p, page_first) : page_row(p, seq, pg);
           if constexpr (kFp8) {
             unsigned char* dst = sm + kOffStage + s * kStageBytes + kRawOffset;
             ptx::mbar_arrive_expect_tx(&bars.stage_full[s], 9 * kRawChunk);
@@ -295,14 +317,15 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
                 ptx::tma_load_2d(dst + c * kPageChunk, &tm_cache, &bars.vpart_full[v], (4 * half + c) * 64, y);
             }
           }
+          if (pg == lo) warm_next_q();
           // warm L2 with the pages ahead (after this page's own load has been issued)
           for (int a = (pg == lo ? lo + 1 : pg + kPrefetchAhead); a <= min(hi - 1, pg + kPrefetchAhead); ++a) {
             const int ya = page_row(p, seq, a);
             if (ya < 0) continue;
-            if (p.page_box)
-              ptx::tma_prefetch_3d(&tm_page, 0, ya, 0);
-            else
-              for (int c = 0; c < 9; ++c) ptx::tma_prefetch_2d(&tm_cache, c * 64, ya);
+            // the page is 72 KB (bf16; 36 KB fp8) of contiguous bytes: one linear prefetch
+            // reads it in address order
+            constexpr uint32_t kPageBytes = kPage * kDc * (kFp8 ? 1 : 2);
+            ptx::bulk_prefetch(p.cache_bytes + (size_t)ya * (kDc * (kFp8 ? 1 : 2)), kPageBytes);
           }
         }
       }
@@ -583,7 +606,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
     // -------------------------------------------------------------- softmax / epilogue
     const int r = threadIdx.x - 128;  // query row == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    int g = 0, n_epi = 0, n_part = 0;
+    int g = 0, n_epi = 0, n_part = 0, n_bulk = 0, n_bulk_issued = 0;
     bool ok = true;
     // a sequence with no cached key is in no work unit's range: unit u writes O = 0 and
     // LSE = -inf for the empty sequences u, u + G, u + 2G, ...
@@ -727,20 +750,43 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
       // read from the accumulator.  Otherwise it writes its partial (O_half / l, LSE), makes
       // it visible device-wide and counts itself in; the split that completes the count
       // merges: O = sum_c exp(lse_c - lse) O_c with lse = ln sum_c exp(lse_c).
+      // After the unit's last segment nothing more is loaded and every MMA is complete: Q's
+      // area takes the staged bf16 output rows, the page stages a bulk copy of the other
+      // split's partial when the sequence has exactly two (one TMA transfer instead of
+      // rounds of dependent L2 loads per thread).
+      bool last_seg;
+      {
+        Segments nx = segs;
+        int s2, L2, lo2, hi2;
+        last_seg = !nx.next(s2, L2, lo2, hi2);
+      }
       if (r == 0) {
-        int fast = 1;
+        int fast = 1, bulk = 0;
         if (nsplit > 1) {
           // the counters were zeroed by the kernel this one was launched behind
           asm volatile("griddepcontrol.wait;" ::: "memory");
           fast = ptx::ld_acquire_gpu(p.counters + (size_t)seq * 2 + half) == nsplit - 1;
+          if (fast && nsplit == 2 && last_seg) {
+            const float4* src = reinterpret_cast<const float4*>(p.part_o) +
+                                ((size_t)(c_first + seq + (1 - k_own)) * 128 + half * 64) * TQ;
+            ptx::fence_proxy_async_global();
+            ptx::mbar_arrive_expect_tx(&bars.merge_full, 1024u * TQ);
+            ptx::bulk_load(sm + kOffStage, src, 1024u * TQ, &bars.merge_full);
+            bulk = 1;
+            ++n_bulk_issued;
+          }
         }
         bars.merge_fast = fast;
+        bars.merge_bulk = bulk;
         ptx::mbar_arrive(&bars.dec_go);
       }
       ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.dec_go, n_epi & 1, abort_flag, p.err));
       ++n_epi;
       if (!ok) break;
-      const bool own_in_tmem = *reinterpret_cast<volatile int*>(&bars.merge_fast) != 0;
+      // The accumulator is intact until the next segment's first PV product, which waits for
+      // this epilogue: a split that merges always takes its own share from it.
+      bool own_in_tmem = *reinterpret_cast<volatile int*>(&bars.merge_fast) != 0;
+      bool bulk = *reinterpret_cast<volatile int*>(&bars.merge_bulk) != 0;
       bool merge = own_in_tmem;
       if (!own_in_tmem) {
         // partial layout [slot][column quad (128)][row (T*H)][4]: the 32 rows of a warp store
@@ -782,6 +828,15 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
             const int done = MLA_STORE_OK(cnt, p.counters, p.counters_bytes, p.err) ? atomicAdd(cnt, 1) + 1 : 0;
             __threadfence();
             bars.merge_last = done == nsplit ? 1 : 0;
+            if (done == nsplit && nsplit == 2 && last_seg) {
+              const float4* src = reinterpret_cast<const float4*>(p.part_o) +
+                                  ((size_t)(c_first + seq + (1 - k_own)) * 128 + half * 64) * TQ;
+              ptx::fence_proxy_async_global();
+              ptx::mbar_arrive_expect_tx(&bars.merge_full, 1024u * TQ);
+              ptx::bulk_load(sm + kOffStage, src, 1024u * TQ, &bars.merge_full);
+              bars.merge_bulk = 1;
+              ++n_bulk_issued;
+            }
           } else {
             bars.merge_last = 0;
           }
@@ -791,76 +846,97 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
         ++n_part;
         if (!ok) break;
         merge = *reinterpret_cast<volatile int*>(&bars.merge_last) != 0;
+        bulk = *reinterpret_cast<volatile int*>(&bars.merge_bulk) != 0;
+        own_in_tmem = merge;
       }
       if (merge) {
         // Every lane of a warp runs this block (the accumulator loads are warp-collective:
         // a lane that skipped them would stall its warp for good); global memory is touched
         // for the live rows only.  This thread's row: weights of the splits from their LSEs
-        // (read through L2: they were written by other SMs during this launch).
+        // (read through L2: they were written by other SMs during this launch).  The first
+        // kLseRegs LSEs are loaded together and kept; any further split's is read again
+        // where it is used.
         const float* lsp = p.part_lse + ((size_t)half * p.n_slots + c_first + seq) * TQ + r;
         auto lse_of = [&](int k) -> float {
           if (own_in_tmem && k == k_own) return lse_own;
           return row_live ? ptx::ld_l2(lsp + (size_t)k * TQ) : -INFINITY;
         };
+        constexpr int kLseRegs = 4;
+        float lse_r[kLseRegs];
+#pragma unroll
+        for (int k = 0; k < kLseRegs; ++k) lse_r[k] = k < nsplit ? lse_of(k) : -INFINITY;
         float mxl = -INFINITY;
-        for (int k = 0; k < nsplit; ++k) mxl = fmaxf(mxl, lse_of(k));
+#pragma unroll
+        for (int k = 0; k < kLseRegs; ++k) mxl = fmaxf(mxl, lse_r[k]);
+        for (int k = kLseRegs; k < nsplit; ++k) mxl = fmaxf(mxl, lse_of(k));
         auto wraw = [&](float ls) { return (mxl == -INFINITY || ls == -INFINITY) ? 0.f : __expf(ls - mxl); };
         float wsum = 0.f;
-        for (int k = 0; k < nsplit; ++k) wsum += wraw(lse_of(k));
+#pragma unroll
+        for (int k = 0; k < kLseRegs; ++k) wsum += wraw(lse_r[k]);
+        for (int k = kLseRegs; k < nsplit; ++k) wsum += wraw(lse_of(k));
         const float winv = wsum > 0.f ? 1.f / wsum : 0.f;
-        const float w_own = own_in_tmem ? wraw(lse_own) * winv * inv : 0.f;  // on the unnormalised O
+        float w_r[kLseRegs];
+#pragma unroll
+        for (int k = 0; k < kLseRegs; ++k) w_r[k] = wraw(lse_r[k]) * winv;
         const float4* src = reinterpret_cast<const float4*>(p.part_o) +
                             ((size_t)(c_first + seq) * 128 + half * 64) * TQ + r;
         const size_t slot_stride = (size_t)128 * TQ;
         uint4* orow = reinterpret_cast<uint4*>(
             p.out + ((size_t)(seq / p.NQT) * TH + gr) * kDl + half * 256);
-        // After the unit's last segment the page stages are free (every PV product is
-        // complete and nothing more is loaded): the bf16 rows are staged there, 512 bytes per
+        // After the unit's last segment the bf16 rows are staged in Q's area, 512 bytes per
         // row with 16-byte chunk c of row r at chunk c ^ (r mod 32), and each warp then stores
         // its 32 rows as one 512-byte run per instruction.  Earlier segments store straight
         // from the row's thread.
-        bool staged;
-        {
-          Segments nx = segs;
-          int s2, L2, lo2, hi2;
-          staged = !nx.next(s2, L2, lo2, hi2);
+        const bool staged = last_seg;
+        unsigned char* stage_out = sm + kOffQhi;
+        // the bulk-copied partial of the other split: [quad][row][4] floats from the stages
+        const float4* part_sm = reinterpret_cast<const float4*>(sm + kOffStage) + r;
+        if (bulk) {
+          ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.merge_full, n_bulk & 1, abort_flag, p.err));
+          ++n_bulk;
+          if (!ok) break;
         }
-        unsigned char* stage_out = sm + kOffStage;
-        // sixteen column quads (64 columns) per round: 16 independent 16-byte loads of a
-        // split's partial in flight
+        // Sixteen column quads (64 columns) per round: 16 independent 16-byte loads of a
+        // split's partial in flight.  The splits are summed in split order, each as weight x
+        // (O_c / l_c) in fp32, the own share formed from the accumulator exactly as its stored
+        // partial would be: the result does not depend on which split merges.
 #pragma unroll 1
         for (int q = 0; q < 64; q += 16) {
           float4 acc[16];
-          if (own_in_tmem) {
-            uint32_t v[2][32];
-            ptx::tmem_ld32(o_addr + q * 4, v[0]);
-            ptx::tmem_ld32(o_addr + q * 4 + 32, v[1]);
-            ptx::tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              acc[j] = make_float4(__uint_as_float(v[j >> 3][4 * (j & 7)]) * w_own,
-                                   __uint_as_float(v[j >> 3][4 * (j & 7) + 1]) * w_own,
-                                   __uint_as_float(v[j >> 3][4 * (j & 7) + 2]) * w_own,
-                                   __uint_as_float(v[j >> 3][4 * (j & 7) + 3]) * w_own);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-          }
+          for (int j = 0; j < 16; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
           for (int k = 0; k < nsplit; ++k) {
-            if (own_in_tmem && k == k_own) continue;
+            const float w = k == 0 ? w_r[0] : k == 1 ? w_r[1] : k == 2 ? w_r[2] : k == 3 ? w_r[3]
+                                                                                 : wraw(lse_of(k)) * winv;
             float4 x[16];
+            if (own_in_tmem && k == k_own) {
+              uint32_t v[2][32];
+              ptx::tmem_ld32(o_addr + q * 4, v[0]);
+              ptx::tmem_ld32(o_addr + q * 4 + 32, v[1]);
+              ptx::tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              x[j] = row_live ? ptx::ld_l2(src + (size_t)k * slot_stride + (size_t)(q + j) * TQ)
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-            const float w = wraw(lse_of(k)) * winv;
+              for (int j = 0; j < 16; ++j)
+                x[j] = make_float4(__uint_as_float(v[j >> 3][4 * (j & 7)]) * inv,
+                                   __uint_as_float(v[j >> 3][4 * (j & 7) + 1]) * inv,
+                                   __uint_as_float(v[j >> 3][4 * (j & 7) + 2]) * inv,
+                                   __uint_as_float(v[j >> 3][4 * (j & 7) + 3]) * inv);
+            } else if (bulk) {  // the other split of two, copied into shared memory
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                x[j] = row_live ? part_sm[(size_t)(q + j) * TQ] : make_float4(0.f, 0.f, 0.f, 0.f);
+            } else {
+              const float4* b = src + (size_t)k * slot_stride;
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                x[j] = row_live ? ptx::ld_l2(b + (size_t)(q + j) * TQ) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              acc[j].x += w * x[j].x;
-              acc[j].y += w * x[j].y;
-              acc[j].z += w * x[j].z;
-              acc[j].w += w * x[j].w;
+              acc[j].x = fmaf(w, x[j].x, acc[j].x);
+              acc[j].y = fmaf(w, x[j].y, acc[j].y);
+              acc[j].z = fmaf(w, x[j].z, acc[j].z);
+              acc[j].w = fmaf(w, x[j].w, acc[j].w);
             }
           }
 #pragma unroll
@@ -894,6 +970,8 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
       // the accumulator was read: the next segment's first PV product may overwrite it
       ptx::tc_fence_before();
     }
+    // after an abort: a bulk copy issued but never waited for lands before the CTA exits
+    if (r == 0 && n_bulk_issued > n_bulk) ptx::mbar_wait_drain(&bars.merge_full, n_bulk & 1);
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -980,6 +1058,7 @@ cudaError_t launch_decode_sm103(const void* q_latent, const void* q_rope, const 
   p.q_latent = static_cast<const uint16_t*>(q_latent);
   p.q_rope = static_cast<const uint16_t*>(q_rope);
   p.kv_scale = kv_scale;
+  p.cache_bytes = static_cast<const unsigned char*>(kv_cache);
   p.page_table = page_table;
   p.cache_lens = cache_lens;
   p.part_o = part_o;

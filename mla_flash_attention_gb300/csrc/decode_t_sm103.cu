@@ -237,6 +237,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long lim = p.wait_limit;
 
   if (threadIdx.x == 0) {
+    // the descriptors are fetched while the barriers are set up and the plan is made
+    ptx::prefetch_tensormap(&tm_s);
+    ptx::prefetch_tensormap(&tm_v);
     bars.abort_flag = 0;
     for (int i = 0; i < kRawSlots; ++i) {
       ptx::mbar_init(&bars.raw_full[i], 1);
@@ -264,12 +267,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(&bars.soft_sync, 4);
     ptx::fence_barrier_init();
   }
+  // the plan's length loads go out first; the other warps set up meanwhile
+  if (warp == 2) make_plan(p, unit, &bars.plan);
   // Q rows TQ..NP-1 are never written: keep the whole Q area zero
   for (int i = threadIdx.x; i < 9 * L_::kQChunk / 16; i += kThreads)
     reinterpret_cast<uint4*>(sm + L_::kOffQ)[i] = make_uint4(0, 0, 0, 0);
   ptx::fence_proxy_async();
   if (warp == 1) ptx::tmem_alloc(&bars.tmem_base, L_::kTmemCols);
-  if (warp == 2) make_plan(p, unit, &bars.plan);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -284,10 +288,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------------------------------- TMA producer
     // The whole warp walks the units; lane 0 arms each raw slot and lanes 0 and 1 issue its
     // (up to) two boxes, so that two tile loads are in issue at once.
-    if (lane == 0) {
-      ptx::prefetch_tensormap(&tm_s);
-      ptx::prefetch_tensormap(&tm_v);
-    }
     int u = 0, last_unit = -1;  // units handed out / the last one whose copies were issued
     bool ok = true;
     // warm L2 with the pages (and their scales) a few blocks ahead of the loads

@@ -243,6 +243,12 @@ __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Order this thread's earlier global-memory accesses (and what it acquired from other
+// threads) before its later async-proxy (bulk copy) reads of global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ tcgen05
 
 // Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format: start address,
