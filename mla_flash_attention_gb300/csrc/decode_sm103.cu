@@ -274,8 +274,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
         };
         for (int pg = lo; pg < hi; ++pg, ++g) {
           const int s = g % kStages;
-          if (!(ok = ptx::mbar_wait(kFp8 ? &bars.stage_empty[s] : &bars.spart_empty,
-                                    kFp8 ? ((g / kStages) & 1) ^ 1 : (g & 1) ^ 1, abort_flag, p.err)))
+          if (kFp8 && !(ok = ptx::mbar_wait(&bars.stage_empty[s], ((g / kStages) & 1) ^ 1, abort_flag, p.err)))
             break;
           // the first sequence's staged Q stays in place until it is copied to TMEM
           if (kFp8 && g == 1 && !(ok = ptx::mbar_wait(&bars.q0_copied, 0, abort_flag, p.err))) break;
@@ -290,8 +289,26 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
                 ptx::tma_load_2d(dst + c * kRawChunk, &tm_cache, &bars.stage_full[s], c * 64, y);
             }
           } else {
-            // score-only chunks in chunk_idx order: half 0 takes 4..8, half 1 0..3 and 8
-            unsigned char* dst = sm + kOffSPart;
+            // The value part first: its slot (the page three back has had its PV) frees about
+            // a page before the score-only slot does, so it goes out then and lands before the
+            // score k-steps reach it, instead of queueing behind this page's score-only part.
+            // Own latent chunks 4 half .. 4 half + 3 (value slots 1 and 2 first hold the first
+            // sequence's staged Q).
+            const int v = g % kVSlots;
+            if (!(ok = ptx::mbar_wait(&bars.vpart_empty[v], ((g / kVSlots) & 1) ^ 1, abort_flag, p.err))) break;
+            if ((g == 1 || g == 2) && !(ok = ptx::mbar_wait(&bars.q0_copied, 0, abort_flag, p.err))) break;
+            unsigned char* dst = sm + kOffVPart + v * kVPartBytes;
+            ptx::mbar_arrive_expect_tx(&bars.vpart_full[v], kVPartBytes);
+            if (p.page_box) {
+              ptx::tma_load_3d(dst, &tm_c4, &bars.vpart_full[v], 0, y, 4 * half);
+            } else {
+              for (int c = 0; c < 4; ++c)
+                ptx::tma_load_2d(dst + c * kPageChunk, &tm_cache, &bars.vpart_full[v], (4 * half + c) * 64, y);
+            }
+            // then the score-only chunks (chunk_idx order: half 0 takes 4..8, half 1 0..3 and
+            // 8), once the previous page's score k-steps over them are done
+            if (!(ok = ptx::mbar_wait(&bars.spart_empty, (g & 1) ^ 1, abort_flag, p.err))) break;
+            dst = sm + kOffSPart;
             ptx::mbar_arrive_expect_tx(&bars.spart_full, kSPartBytes);
             if (p.page_box && half == 0) {
               ptx::tma_load_3d(dst, &tm_c5, &bars.spart_full, 0, y, 4);
@@ -302,19 +319,6 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
               for (int i = 0; i < 5; ++i)
                 ptx::tma_load_2d(dst + i * kPageChunk, &tm_cache, &bars.spart_full,
                                  (half == 0 ? 4 + i : (i < 4 ? i : 8)) * 64, y);
-            }
-            // own latent chunks 4 half .. 4 half + 3, once the page three back has had its PV
-            // (value slots 1 and 2 first hold the first sequence's staged Q)
-            const int v = g % kVSlots;
-            if (!(ok = ptx::mbar_wait(&bars.vpart_empty[v], ((g / kVSlots) & 1) ^ 1, abort_flag, p.err))) break;
-            if ((g == 1 || g == 2) && !(ok = ptx::mbar_wait(&bars.q0_copied, 0, abort_flag, p.err))) break;
-            dst = sm + kOffVPart + v * kVPartBytes;
-            ptx::mbar_arrive_expect_tx(&bars.vpart_full[v], kVPartBytes);
-            if (p.page_box) {
-              ptx::tma_load_3d(dst, &tm_c4, &bars.vpart_full[v], 0, y, 4 * half);
-            } else {
-              for (int c = 0; c < 4; ++c)
-                ptx::tma_load_2d(dst + c * kPageChunk, &tm_cache, &bars.vpart_full[v], (4 * half + c) * 64, y);
             }
           }
           if (pg == lo) warm_next_q();
