@@ -10,9 +10,10 @@
 //
 // Per CTA (8 warps; 12 with the fp8 cache):
 //   warp 0      TMA producer: each sequence's Q latent 0..255 (staged in shared memory),
-//               then one cache page (64 keys x 576 columns) per stage, as nine 64-column
-//               chunks -- bf16: 128B-swizzled, ready for the MMA; fp8: raw bytes into the
-//               upper half of the stage -- plus L2 prefetch of pages ahead
+//               then the cache pages (64 keys x 576 columns) -- bf16: in two parts, the
+//               five score-only 64-column chunks and the CTA's four value chunks, 128B-
+//               swizzled, ready for the MMA; fp8: the whole raw page into the upper half of
+//               a stage -- plus L2 prefetch of pages ahead
 //   warp 1      MMA issuer: at a sequence change, copies the staged Q latent 0..255 into
 //               TMEM (tcgen05.cp) and loads latent 256..511 + rope into shared memory by TMA;
 //               then S(g) = Q C(g)' into one of two S buffers (A operand = Q: latent 0..255
@@ -229,9 +230,10 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
 
   if (warp == 0) {
     // -------------------------------------------------------------- TMA producer
-    // One lane issues Q, the pages in order (fp8: whole pages; bf16: the score-only part, then
-    // the value part, which is released later) and the L2 warming.  Copies are served in
-    // issue order, so a page's value part never waits behind the next page's score-only part.
+    // One lane issues Q, the pages in order (fp8: whole pages; bf16: the value part as soon
+    // as its ring slot frees, then the score-only part once the previous page's scores are
+    // done with that slot) and the L2 warming.  Copies are served in issue order, so the
+    // value part, which goes out about a page earlier, never waits behind a score-only part.
     if ((threadIdx.x & 31) == 0) {
       int g = 0, nseg = 0;
       bool ok = true;
