@@ -75,10 +75,11 @@ def fp8_prefill_roofline(pairs, ms, pk):
     Q_nope K_nope' 2*128 FLOP and P V 2*128 FLOP with fp8 inputs, Q_rope K_rope' 2*64 FLOP in
     bf16.  fp8-input roofline: the fp8 FLOP at the fp8 peak plus the rope FLOP at the bf16
     peak.  Issued-precision roofline: as the kernel issues them -- nope scores on fp8, rope on
-    bf16, and P V as two bf16 products (the high and low bf16 parts of P' = p ks)."""
+    bf16, and P V as one f16 product (P'' = p ks in f16 against V widened to f16), at the
+    16-bit rate."""
     f_nope, f_rope, f_pv = 2.0 * 128 * pairs, 2.0 * 64 * pairs, 2.0 * 128 * pairs
     t_in = (f_nope + f_pv) / (pk["fp8_tflops"] * 1e12) + f_rope / (pk["bf16_tflops"] * 1e12)
-    t_issued = f_nope / (pk["fp8_tflops"] * 1e12) + (f_rope + 2 * f_pv) / (pk["bf16_tflops"] * 1e12)
+    t_issued = f_nope / (pk["fp8_tflops"] * 1e12) + (f_rope + f_pv) / (pk["bf16_tflops"] * 1e12)
     t = ms * 1e-3
     return {"flop_split": {"fp8_nope_scores": f_nope, "bf16_rope_scores": f_rope, "fp8_pv": f_pv},
             "roofline_ms_fp8_input": t_in * 1e3, "frac_fp8_input": t_in / t,
