@@ -13,10 +13,11 @@
 // of p (exact up to fp32 rounding); O is accumulated in fp32 and written in fp32 by default.
 //
 // One CTA = (batch, head, 256 query rows) as two 128-row Q tiles; keys in tiles of 64.  Each
-// Q tile has its own score buffers (Sn, Sr: 64 + 64 TMEM columns, P'' written over Sn) and
+// Q tile has its own score buffers (Sn, Sr: 64 + 64 TMEM columns, P'' written over Sr) and
 // O (128 columns): 2 x 256 = 512 TMEM columns.  The MMA warp interleaves the tiles
-// (PV_0(j), S_0(j+1), PV_1(j), S_1(j+1)) so one softmax warpgroup works while the tensor
-// core serves the other.  Warps: 0 TMA producer (3-stage rings), 1 MMA issuer, 2-3
+// (Sn_0(j+1), PV_0(j), Sr_0(j+1), then the same for tile 1), each tile's next nope scores
+// going out as soon as its softmax has read S(j), so one softmax warpgroup works while the
+// tensor core serves the other.  Warps: 0 TMA producer (3-stage rings), 1 MMA issuer, 2-3
 // converters (V8 -> f16 N-major tile, key scales into shared memory; warp 2 also owns the
 // TMEM allocation), 4-7 softmax of Q tile 0, 8-11 softmax of Q tile 1 (one thread per row).
 #include <cuda.h>
@@ -66,7 +67,7 @@ struct Bars {
   uint64_t k_full[kStages], k_empty[kStages];
   uint64_t v8_full[kStages], v8_empty[kStages], vh_full[kStages], vh_empty[kStages];
   uint64_t ks_full[kStages];
-  uint64_t s_full[NQ], p_full[NQ], o_done[NQ];
+  uint64_t s_full[NQ], s_read[NQ], p_full[NQ], o_done[NQ];
   uint32_t tmem_base;
   int abort_flag;
   float ks[kStages][BN];    // the key tile's dequantisation scales
@@ -118,6 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; t < NQ; ++t) {
       ptx::mbar_init(&bars.s_full[t], 1);
       ptx::mbar_init(&bars.p_full[t], 4);  // one arrival per softmax warp of the tile
+      ptx::mbar_init(&bars.s_read[t], 4);
       ptx::mbar_init(&bars.o_done[t], 1);
     }
     ptx::fence_barrier_init();
@@ -161,20 +163,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       // S_t(j): Sn_t over the nope depth (K = 128 fp8 = 4 x 32), Sr_t over the rope depth
       // (K = 64 bf16 = 4 x 16); TMEM columns of tile t: [256t, 256t+64) Sn (then P''),
       // [256t+64, 256t+128) Sr, [256t+128, 256t+256) O
-      auto issue_s = [&](int t, int j) {
+      auto issue_sn = [&](int t, int j) {
         const int s = j % kStages;
-        const uint32_t dn = tmem + t * 256, dr = dn + 64;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const uint64_t da = ptx::sw128_desc(qn + t * kQChunk + k * 32, 16, 1024);
           const uint64_t db = ptx::sw128_desc(kn + s * kKChunk + k * 32, 16, 1024);
-          ptx::mma_f8_ss(dn, da, db, kIdSn, k > 0);
+          ptx::mma_f8_ss(tmem + t * 256, da, db, kIdSn, k > 0);
         }
+      };
+      auto issue_sr = [&](int t, int j) {
+        const int s = j % kStages;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const uint64_t da = ptx::sw128_desc(qr + t * kQChunk + k * 32, 16, 1024);
           const uint64_t db = ptx::sw128_desc(kr + s * kKChunk + k * 32, 16, 1024);
-          ptx::mma_bf16_ss(dr, da, db, kIdSr, k > 0);
+          ptx::mma_bf16_ss(tmem + t * 256 + 64, da, db, kIdSr, k > 0);
         }
       };
       auto wait_k = [&](int j) -> bool {
@@ -189,16 +193,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const uint64_t db = ptx::sw128_desc(v + k * 2048, kKChunk, 1024);
-          ptx::mma_bf16_ts(tmem + t * 256 + 128, tmem + t * 256 + k * 8, db, kIdPV, (j > 0 || k > 0) ? 1u : 0u);
+          ptx::mma_bf16_ts(tmem + t * 256 + 128, tmem + t * 256 + 64 + k * 8, db, kIdPV, (j > 0 || k > 0) ? 1u : 0u);
         }
         return true;
       };
+      // Per key tile j and Q tile t: the nope scores of tile j + 1 go out as soon as the
+      // softmax has read S_t(j) (their columns are then free), the PV product on P''_t(j)
+      // (written over Sr_t), then the rope scores of j + 1 over it; the two Q tiles interleave.
       if (ok && n_kv > 0 && (ok = wait_k(0))) {
         ptx::tc_fence_after();
-        issue_s(0, 0);
-        ptx::mma_commit(&bars.s_full[0]);
-        issue_s(1, 0);
-        ptx::mma_commit(&bars.s_full[1]);
+        for (int t = 0; t < NQ; ++t) {
+          issue_sn(t, 0);
+          issue_sr(t, 0);
+          ptx::mma_commit(&bars.s_full[t]);
+        }
         ptx::mma_commit(&bars.k_empty[0]);
       }
       for (int j = 0; ok && j < n_kv; ++j) {
@@ -207,25 +215,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool more = j + 1 < n_kv;
         bool k_ready = false;
         if (j < n_kv0) {
+          const bool next0 = j + 1 < n_kv0;
+          if (next0) {
+            if (!(ok = wait_k(j + 1))) break;
+            k_ready = true;
+            if (!(ok = ptx::mbar_wait(&bars.s_read[0], j & 1, abort_flag, p.err))) break;
+            ptx::tc_fence_after();
+            issue_sn(0, j + 1);
+          }
           if (!(ok = issue_pv(0, j))) break;
           ptx::mma_commit(&bars.o_done[0]);
-          if (j + 1 < n_kv0) {
-            if (!(ok = wait_k(j + 1))) break;
-            ptx::tc_fence_after();
-            k_ready = true;
-            issue_s(0, j + 1);
+          if (next0) {
+            issue_sr(0, j + 1);
             ptx::mma_commit(&bars.s_full[0]);
           }
+        }
+        if (more) {
+          if (!k_ready && !(ok = wait_k(j + 1))) break;
+          if (!(ok = ptx::mbar_wait(&bars.s_read[1], j & 1, abort_flag, p.err))) break;
+          ptx::tc_fence_after();
+          issue_sn(1, j + 1);
         }
         if (!(ok = issue_pv(1, j))) break;
         ptx::mma_commit(&bars.o_done[1]);
         ptx::mma_commit(&bars.vh_empty[s]);
         if (more) {
-          if (!k_ready) {
-            if (!(ok = wait_k(j + 1))) break;
-            ptx::tc_fence_after();
-          }
-          issue_s(1, j + 1);
+          issue_sr(1, j + 1);
           ptx::mma_commit(&bars.s_full[1]);
           ptx::mma_commit(&bars.k_empty[(j + 1) % kStages]);
         }
@@ -317,6 +332,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           u2[hf * 16 + x] = ptx::fma2(s2[hf * 16 + x], c2, ptx::f2(lks[k], lks[k + 1]));
         }
       }
+      // S_t(j) is in registers: the MMA warp may write the next tile's nope scores
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&bars.s_read[t]);
       const int key0 = j * BN;
       if ((key0 + BN > p.S) || (p.causal && key0 + BN - 1 > q_row0 + t * BM)) {
         const int lim = p.causal ? min(i + 1, p.S) : p.S;  // keys < lim are visible
@@ -373,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t w2 = ptx::mul2(pp, ptx::f2(ks[2 * x], ks[2 * x + 1]));
         pk[x] = ptx::pack_f16x2(ptx::f2_lo(w2), ptx::f2_hi(w2));
       }
-      ptx::tmem_st32(sn_addr, pk);
+      ptx::tmem_st32(sn_addr + 64, pk);  // over Sr_t
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       __syncwarp();
