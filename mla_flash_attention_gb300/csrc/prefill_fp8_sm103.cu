@@ -23,6 +23,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstddef>
+
 #include "common.cuh"
 #include "sm103_ptx.cuh"
 
@@ -70,9 +72,12 @@ struct Bars {
   uint64_t s_full[NQ], s_read[NQ], p_full[NQ], o_done[NQ];
   uint32_t tmem_base;
   int abort_flag;
-  float ks[kStages][BN];    // the key tile's dequantisation scales
-  float lks[kStages][BN];   // max(log2 ks, kLog2KsFloor)
+  // read 16 bytes at a time by the softmax warps (one shared-memory wavefront per four keys)
+  alignas(16) float ks[kStages][BN];    // the key tile's dequantisation scales
+  alignas(16) float lks[kStages][BN];   // max(log2 ks, kLog2KsFloor)
 };
+static_assert(offsetof(Bars, ks) % 16 == 0 && offsetof(Bars, lks) % 16 == 0 && (BN * 4) % 16 == 0,
+              "the key-scale rows are read 16 bytes at a time");
 
 __device__ __forceinline__ int n_kv_tiles(const Params& p, int rows_end) {
   const int all = (p.S + BN - 1) / BN;
@@ -311,8 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_after();
       ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars.ks_full[j % kStages], (j / kStages) & 1, abort_flag, p.err));
       if (!ok) break;
-      const float* ks = bars.ks[j % kStages];
-      const float* lks = bars.lks[j % kStages];
+      const float4* ks4 = reinterpret_cast<const float4*>(bars.ks[j % kStages]);
+      const float4* lks4 = reinterpret_cast<const float4*>(bars.lks[j % kStages]);
       // scores s = qs ks Sn + Sr and exponents u = c s + log2 ks, two keys per packed
       // instruction, 32 keys per half
       uint64_t s2[32], u2[32];
@@ -323,13 +328,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_ld32(sn_addr + 64 + hf * 32, vr);
         ptx::tmem_ld_wait();
 #pragma unroll
-        for (int x = 0; x < 16; ++x) {
-          const int k = hf * 32 + 2 * x;
-          const uint64_t ks2 = ptx::f2(ks[k], ks[k + 1]);
-          s2[hf * 16 + x] = ptx::fma2(ptx::f2(__uint_as_float(vn[2 * x]), __uint_as_float(vn[2 * x + 1])),
-                                      ptx::mul2(qs2, ks2),
-                                      ptx::f2(__uint_as_float(vr[2 * x]), __uint_as_float(vr[2 * x + 1])));
-          u2[hf * 16 + x] = ptx::fma2(s2[hf * 16 + x], c2, ptx::f2(lks[k], lks[k + 1]));
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const float4 kq = ks4[hf * 8 + q4], lq = lks4[hf * 8 + q4];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int x = 2 * q4 + e;  // key pair within the half
+            const uint64_t ks2 = e == 0 ? ptx::f2(kq.x, kq.y) : ptx::f2(kq.z, kq.w);
+            const uint64_t lks2 = e == 0 ? ptx::f2(lq.x, lq.y) : ptx::f2(lq.z, lq.w);
+            s2[hf * 16 + x] = ptx::fma2(ptx::f2(__uint_as_float(vn[2 * x]), __uint_as_float(vn[2 * x + 1])),
+                                        ptx::mul2(qs2, ks2),
+                                        ptx::f2(__uint_as_float(vr[2 * x]), __uint_as_float(vr[2 * x + 1])));
+            u2[hf * 16 + x] = ptx::fma2(s2[hf * 16 + x], c2, lks2);
+          }
         }
       }
       // S_t(j) is in registers: the MMA warp may write the next tile's nope scores
@@ -385,12 +395,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // p = 2^(c s - m) (fp32; the row sum), P'' = p ks in f16 over Sn (the PV weight)
       uint32_t pk[32];
 #pragma unroll
-      for (int x = 0; x < 32; ++x) {
-        const uint64_t a2 = ptx::fma2(s2[x], c2, nm2);
-        const uint64_t pp = ptx::f2(ptx::ex2(ptx::f2_lo(a2)), ptx::ex2(ptx::f2_hi(a2)));
-        l2 = ptx::add2(l2, pp);
-        const uint64_t w2 = ptx::mul2(pp, ptx::f2(ks[2 * x], ks[2 * x + 1]));
-        pk[x] = ptx::pack_f16x2(ptx::f2_lo(w2), ptx::f2_hi(w2));
+      for (int q4 = 0; q4 < 16; ++q4) {
+        const float4 kq = ks4[q4];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int x = 2 * q4 + e;
+          const uint64_t a2 = ptx::fma2(s2[x], c2, nm2);
+          const uint64_t pp = ptx::f2(ptx::ex2(ptx::f2_lo(a2)), ptx::ex2(ptx::f2_hi(a2)));
+          l2 = ptx::add2(l2, pp);
+          const uint64_t w2 = ptx::mul2(pp, e == 0 ? ptx::f2(kq.x, kq.y) : ptx::f2(kq.z, kq.w));
+          pk[x] = ptx::pack_f16x2(ptx::f2_lo(w2), ptx::f2_hi(w2));
+        }
       }
       ptx::tmem_st32(sn_addr + 64, pk);  // over Sr_t
       ptx::tmem_st_wait();
