@@ -166,8 +166,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t vh = ptx::smem_u32(sm + kOffVh);
       bool ok = ptx::mbar_wait(&bars.q_full, 0, abort_flag, p.err);
       // S_t(j): Sn_t over the nope depth (K = 128 fp8 = 4 x 32), Sr_t over the rope depth
-      // (K = 64 bf16 = 4 x 16); TMEM columns of tile t: [256t, 256t+64) Sn (then P''),
-      // [256t+64, 256t+128) Sr, [256t+128, 256t+256) O
+      // (K = 64 bf16 = 4 x 16); TMEM columns of tile t: [256t, 256t+64) Sn,
+      // [256t+64, 256t+128) Sr (P'' in its first 32), [256t+128, 256t+256) O
       auto issue_sn = [&](int t, int j) {
         const int s = j % kStages;
 #pragma unroll
@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto wait_k = [&](int j) -> bool {
         return ptx::mbar_wait(&bars.k_full[j % kStages], (j / kStages) & 1, abort_flag, p.err);
       };
-      // O_t (+)= P''_t(j) V(j): P'' (f16 pairs, 32 TMEM columns over Sn_t), 4 k-steps of 16
+      // O_t (+)= P''_t(j) V(j): P'' (f16 pairs, 32 TMEM columns over Sr_t), 4 k-steps of 16
       // keys; B = the f16 V tile, N-major (two 64-column chunks 8 KB apart)
       auto issue_pv = [&](int t, int j) -> bool {
         if (!ptx::mbar_wait(&bars.p_full[t], j & 1, abort_flag, p.err)) return false;
@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = (warp & 3) * 32 + lane;   // row within the tile == TMEM lane
     const int i = q_row0 + t * BM + r;      // query index
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t sn_addr = tmem + lane_off + t * 256;  // Sn, then P''
+    const uint32_t sn_addr = tmem + lane_off + t * 256;  // Sn; Sr (then P'') at + 64
     const uint32_t o_addr = sn_addr + 128;
     const float qs = i < p.S ? __ldg(p.q_scale + (size_t)b * p.S + i) : 0.f;
     const uint64_t qs2 = ptx::f2(qs, qs), c2 = ptx::f2(p.scale_log2, p.scale_log2);
@@ -392,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       m = m_use;
       const float neg_m = (m == -INFINITY) ? 0.f : -m;
       const uint64_t nm2 = ptx::f2(neg_m, neg_m);
-      // p = 2^(c s - m) (fp32; the row sum), P'' = p ks in f16 over Sn (the PV weight)
+      // p = 2^(c s - m) (fp32; the row sum), P'' = p ks in f16 over Sr (the PV weight)
       uint32_t pk[32];
 #pragma unroll
       for (int q4 = 0; q4 < 16; ++q4) {
