@@ -171,21 +171,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t q_base = ptx::smem_u32(sm + kOffQ);
       const uint32_t ring_base = ptx::smem_u32(sm + kOffRing);
       const uint32_t rope_base = ptx::smem_u32(sm + kOffRope);
+      // operand descriptors built once; a tile at a byte offset from its base differs only in
+      // the start-address field (address / 16, no carry below 256 KB)
+      const uint64_t d_q = ptx::sw128_desc(q_base, 16, 1024);
+      const uint64_t d_ring = ptx::sw128_desc(ring_base, 16, 1024);
+      const uint64_t d_rope = ptx::sw128_desc(rope_base, 16, 1024);
+      const uint64_t d_v = ptx::sw128_desc(ring_base, kChunk, 1024);
+      // (an opaque add, so the compiler forms each descriptor where it is used instead of
+      // keeping all of them live)
+      auto at = [](uint64_t d, uint32_t bytes) {
+        uint64_t r;
+        asm volatile("add.u64 %0, %1, %2;" : "=l"(r) : "l"(d), "l"(static_cast<uint64_t>(bytes >> 4)));
+        return r;
+      };
       bool ok = ptx::mbar_wait(&bars.q_full, 0, abort_flag, p.err);
 
       // S_t(j) = Q_t K(j)': 8 k-steps over the nope chunks + 4 over the rope chunk
       auto issue_s = [&](int t, int j) {
         const int ks = (2 * j) % kRingSlots, rs = j % kRopeSlots;
-        const uint32_t qa = q_base + t * kQTile;
-        const uint32_t kb = ring_base + ks * 2 * kChunk;
-        const uint32_t rb_ = rope_base + rs * kChunk;
+        const uint64_t qa = at(d_q, t * kQTile);
+        const uint64_t kb = at(d_ring, ks * 2 * kChunk);
+        const uint64_t rb_ = at(d_rope, rs * kChunk);
         const uint32_t d = tmem + t * BN;
 #pragma unroll
         for (int k = 0; k < 12; ++k) {
           const int c = k >> 2, kk = k & 3;
-          const uint64_t da = ptx::sw128_desc(qa + c * kChunk + kk * 32, 16, 1024);
-          const uint32_t baddr = (c < 2 ? kb + c * kChunk : rb_) + kk * 32;
-          const uint64_t db = ptx::sw128_desc(baddr, 16, 1024);
+          const uint64_t da = at(qa, c * kChunk + kk * 32);
+          const uint64_t db = c < 2 ? at(kb, c * kChunk + kk * 32) : at(rb_, kk * 32);
           ptx::mma_bf16_ss(d, da, db, kIdS, k > 0);
         }
       };
@@ -198,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // PV in two halves of 64 keys, each issued as soon as that half of P is in TMEM
       auto issue_pv = [&](int t, int j) -> bool {
         const int vs = (2 * j + 1) % kRingSlots;
-        const uint32_t vb = ring_base + vs * 2 * kChunk;
+        const uint64_t vb = at(d_v, vs * 2 * kChunk);
         const uint32_t d = tmem + 2 * BN + t * 128;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
@@ -206,8 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tc_fence_after();
 #pragma unroll
           for (int k = 4 * hf; k < 4 * hf + 4; ++k) {
-            const uint64_t db = ptx::sw128_desc(vb + k * 2048, kChunk, 1024);
-            ptx::mma_bf16_ts(d, tmem + t * BN + k * 8, db, kIdPV, (j > 0 || k > 0) ? 1u : 0u);
+            ptx::mma_bf16_ts(d, tmem + t * BN + k * 8, at(vb, k * 2048), kIdPV, (j > 0 || k > 0) ? 1u : 0u);
           }
         }
         return true;
