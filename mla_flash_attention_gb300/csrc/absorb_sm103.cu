@@ -4,7 +4,8 @@
 //
 // (q_latent = q_nope W_UK[h] before decode: K = 128, N = 512; o = O_latent W_UV[h] after
 // it: K = 512, N = 128.)  One CTA per (128-row tile of r, 128 columns of n, head h), 4 warps:
-// warp 0 (one lane) streams K in 64-deep chunks by TMA through a 2-stage ring (x chunk
+// warp 0 (one lane) streams K in 64-deep chunks by TMA through a ring of min(K / 64, 6)
+// stages, so a deep contraction keeps most of its chunks in flight at once (x chunk
 // 128 rows x 64 K-major, w chunk 64 K-rows x 128 columns N-major, both 128B-swizzled);
 // warp 1 (one lane) issues the bf16 MMAs (M = N = 128, K = 16) into a 128-column fp32 TMEM
 // accumulator; then every thread takes one row of it to bf16 and stores 256 bytes.
@@ -17,17 +18,18 @@
 namespace mla {
 namespace sm103_absorb {
 
-constexpr int BM = 128, BN = 128, BK = 64, kStages = 2;
+constexpr int BM = 128, BN = 128, BK = 64, kMaxStages = 6;
 constexpr int kAChunk = BM * 128;               // 128 rows x 64 bf16
 constexpr int kBHalf = BK * 128;                // 64 K-rows x 64 bf16 (one 64-column half)
 constexpr int kStageBytes = kAChunk + 2 * kBHalf;  // 32 KB
-constexpr int kSmemAlloc = kStages * kStageBytes + 1024;
+constexpr int kSmemMax = kMaxStages * kStageBytes + 1024;  // 193 KB
 constexpr int kThreads = 128;
 
 struct Params {
   uint16_t* y;
   unsigned int* err;
   int R, H, K, N;
+  int stages;  // ring depth, min(K / BK, kMaxStages)
 };
 
 __global__ void __launch_bounds__(kThreads) absorb_kernel(const __grid_constant__ CUtensorMap tm_x,
@@ -36,7 +38,7 @@ __global__ void __launch_bounds__(kThreads) absorb_kernel(const __grid_constant_
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  __shared__ uint64_t full[kStages], empty[kStages], done;
+  __shared__ uint64_t full[kMaxStages], empty[kMaxStages], done;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -45,7 +47,7 @@ __global__ void __launch_bounds__(kThreads) absorb_kernel(const __grid_constant_
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < p.stages; ++s) {
       ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], 1);
     }
@@ -64,8 +66,8 @@ __global__ void __launch_bounds__(kThreads) absorb_kernel(const __grid_constant_
       ptx::prefetch_tensormap(&tm_x);
       ptx::prefetch_tensormap(&tm_w);
       for (int kc = 0; kc < nk; ++kc) {
-        const int s = kc % kStages;
-        if (!ptx::mbar_wait(&empty[s], ((kc / kStages) & 1) ^ 1, abort_ptr, p.err)) break;
+        const int s = kc % p.stages;
+        if (!ptx::mbar_wait(&empty[s], ((kc / p.stages) & 1) ^ 1, abort_ptr, p.err)) break;
         unsigned char* st = sm + s * kStageBytes;
         ptx::mbar_arrive_expect_tx(&full[s], kStageBytes);
         ptx::tma_load_3d(st, &tm_x, &full[s], kc * BK, h, m0);
@@ -80,8 +82,8 @@ __global__ void __launch_bounds__(kThreads) absorb_kernel(const __grid_constant_
       const uint32_t s0 = ptx::smem_u32(sm);
       bool ok = true;
       for (int kc = 0; kc < nk && ok; ++kc) {
-        const int s = kc % kStages;
-        if (!(ok = ptx::mbar_wait(&full[s], (kc / kStages) & 1, abort_ptr, p.err))) break;
+        const int s = kc % p.stages;
+        if (!(ok = ptx::mbar_wait(&full[s], (kc / p.stages) & 1, abort_ptr, p.err))) break;
         ptx::tc_fence_after();
         const uint32_t a = s0 + s * kStageBytes, b = a + kAChunk;
 #pragma unroll
@@ -151,7 +153,7 @@ cudaError_t launch_absorb_sm103(const void* x, const void* w, void* y, int R, in
       (e = encode_tensor_map(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w, wd, ws, wb)) != cudaSuccess)
     return e;
   static unsigned long long smem_set = 0;
-  if ((e = smem_attr_once(absorb_kernel, kSmemAlloc, &smem_set)) != cudaSuccess) return e;
+  if ((e = smem_attr_once(absorb_kernel, kSmemMax, &smem_set)) != cudaSuccess) return e;
   Params p;
   p.y = static_cast<uint16_t*>(y);
   p.err = err;
@@ -159,8 +161,10 @@ cudaError_t launch_absorb_sm103(const void* x, const void* w, void* y, int R, in
   p.H = H;
   p.K = K;
   p.N = N;
+  p.stages = K / BK < kMaxStages ? K / BK : kMaxStages;
+  if (p.stages < 1) return cudaErrorInvalidValue;
   dim3 grid((R + BM - 1) / BM, N / BN, H);
-  absorb_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(tx, tw, p);
+  absorb_kernel<<<grid, kThreads, p.stages * kStageBytes + 1024, stream>>>(tx, tw, p);
   return cudaGetLastError();
 }
 
