@@ -38,6 +38,7 @@ def to_dev(bits):
     (1, 3, 64, 128),       # a single row, the smallest depths
     (130, 5, 192, 256),    # two row tiles with a ragged tail, 3 K chunks, 2 column tiles
     (300, 2, 1024, 128),   # long contraction
+    (17, 2, 128, 384),     # N not a multiple of 256: 128-column tiles
 ])
 def test_absorb_matches_oracle(lib, R, H, K, N):
     x, w = case(R, H, K, N, seed=R * 7 + K)
