@@ -318,15 +318,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       const float4* ks4 = reinterpret_cast<const float4*>(bars.ks[j % kStages]);
       const float4* lks4 = reinterpret_cast<const float4*>(bars.lks[j % kStages]);
-      // scores s = qs ks Sn + Sr and exponents u = c s + log2 ks, two keys per packed
-      // instruction, 32 keys per half
-      uint64_t s2[32], u2[32];
+      // scores s = qs ks Sn + Sr and the running maxima of u = c s + log2 ks (four chains),
+      // two keys per packed instruction, 32 keys per half
+      uint64_t s2[32];
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      const int key0 = j * BN;
+      const bool need_mask = (key0 + BN > p.S) || (p.causal && key0 + BN - 1 > q_row0 + t * BM);
+      const int lim = p.causal ? min(i + 1, p.S) : p.S;  // keys < lim are visible
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         uint32_t vn[32], vr[32];
         ptx::tmem_ld32(sn_addr + hf * 32, vn);
         ptx::tmem_ld32(sn_addr + 64 + hf * 32, vr);
         ptx::tmem_ld_wait();
+        if (need_mask) {  // masked keys: Sn = 0, Sr = -inf, so s = u = -inf
+#pragma unroll
+          for (int y = 0; y < 32; ++y)
+            if (key0 + hf * 32 + y >= lim) {
+              vn[y] = 0u;
+              vr[y] = __float_as_uint(-INFINITY);
+            }
+        }
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4) {
           const float4 kq = ks4[hf * 8 + q4], lq = lks4[hf * 8 + q4];
@@ -338,7 +350,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             s2[hf * 16 + x] = ptx::fma2(ptx::f2(__uint_as_float(vn[2 * x]), __uint_as_float(vn[2 * x + 1])),
                                         ptx::mul2(qs2, ks2),
                                         ptx::f2(__uint_as_float(vr[2 * x]), __uint_as_float(vr[2 * x + 1])));
-            u2[hf * 16 + x] = ptx::fma2(s2[hf * 16 + x], c2, lks2);
+            const uint64_t u = ptx::fma2(s2[hf * 16 + x], c2, lks2);
+            mx4[x & 3] = ptx::fmax3(mx4[x & 3], ptx::f2_lo(u), ptx::f2_hi(u));
           }
         }
       }
@@ -346,19 +359,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&bars.s_read[t]);
-      const int key0 = j * BN;
-      if ((key0 + BN > p.S) || (p.causal && key0 + BN - 1 > q_row0 + t * BM)) {
-        const int lim = p.causal ? min(i + 1, p.S) : p.S;  // keys < lim are visible
-#pragma unroll
-        for (int x = 0; x < 32; ++x) {
-          const bool v0 = key0 + 2 * x < lim, v1 = key0 + 2 * x + 1 < lim;
-          s2[x] = ptx::f2(v0 ? ptx::f2_lo(s2[x]) : -INFINITY, v1 ? ptx::f2_hi(s2[x]) : -INFINITY);
-          u2[x] = ptx::f2(v0 ? ptx::f2_lo(u2[x]) : -INFINITY, v1 ? ptx::f2_hi(u2[x]) : -INFINITY);
-        }
-      }
-      float mx4[4] = {ptx::f2_lo(u2[0]), ptx::f2_hi(u2[0]), ptx::f2_lo(u2[1]), ptx::f2_hi(u2[1])};
-#pragma unroll
-      for (int x = 2; x < 32; ++x) mx4[x & 3] = ptx::fmax3(mx4[x & 3], ptx::f2_lo(u2[x]), ptx::f2_hi(u2[x]));
       const float mx = ptx::fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]);
       float m_use = m;
       if (j == 0) {
