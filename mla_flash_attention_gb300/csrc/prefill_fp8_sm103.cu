@@ -164,6 +164,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t qn = ptx::smem_u32(sm + kOffQn), qr = ptx::smem_u32(sm + kOffQr);
       const uint32_t kn = ptx::smem_u32(sm + kOffKn), kr = ptx::smem_u32(sm + kOffKr);
       const uint32_t vh = ptx::smem_u32(sm + kOffVh);
+      const uint64_t dqn = ptx::sw128_desc(qn, 16, 1024), dqr = ptx::sw128_desc(qr, 16, 1024);
+      const uint64_t dkn = ptx::sw128_desc(kn, 16, 1024), dkr = ptx::sw128_desc(kr, 16, 1024);
+      const uint64_t dvh = ptx::sw128_desc(vh, kKChunk, 1024);
+      // operand descriptors built once; a tile at a byte offset from its base differs only in
+      // the start-address field (address / 16, no carry below 256 KB)
+      auto at = [](uint64_t d, uint32_t bytes) { return d + (bytes >> 4); };
       bool ok = ptx::mbar_wait(&bars.q_full, 0, abort_flag, p.err);
       // S_t(j): Sn_t over the nope depth (K = 128 fp8 = 4 x 32), Sr_t over the rope depth
       // (K = 64 bf16 = 4 x 16); TMEM columns of tile t: [256t, 256t+64) Sn,
@@ -172,18 +178,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = j % kStages;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const uint64_t da = ptx::sw128_desc(qn + t * kQChunk + k * 32, 16, 1024);
-          const uint64_t db = ptx::sw128_desc(kn + s * kKChunk + k * 32, 16, 1024);
-          ptx::mma_f8_ss(tmem + t * 256, da, db, kIdSn, k > 0);
+          ptx::mma_f8_ss(tmem + t * 256, at(dqn, t * kQChunk + k * 32), at(dkn, s * kKChunk + k * 32), kIdSn, k > 0);
         }
       };
       auto issue_sr = [&](int t, int j) {
         const int s = j % kStages;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const uint64_t da = ptx::sw128_desc(qr + t * kQChunk + k * 32, 16, 1024);
-          const uint64_t db = ptx::sw128_desc(kr + s * kKChunk + k * 32, 16, 1024);
-          ptx::mma_bf16_ss(tmem + t * 256 + 64, da, db, kIdSr, k > 0);
+          ptx::mma_bf16_ss(tmem + t * 256 + 64, at(dqr, t * kQChunk + k * 32), at(dkr, s * kKChunk + k * 32), kIdSr, k > 0);
         }
       };
       auto wait_k = [&](int j) -> bool {
@@ -194,12 +196,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_pv = [&](int t, int j) -> bool {
         if (!ptx::mbar_wait(&bars.p_full[t], j & 1, abort_flag, p.err)) return false;
         ptx::tc_fence_after();
-        const uint32_t v = vh + (j % kStages) * 2 * kKChunk;
+        const uint32_t v = (j % kStages) * 2 * kKChunk;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint64_t db = ptx::sw128_desc(v + k * 2048, kKChunk, 1024);
-          ptx::mma_bf16_ts(tmem + t * 256 + 128, tmem + t * 256 + 64 + k * 8, db, kIdPV, (j > 0 || k > 0) ? 1u : 0u);
-        }
+        for (int k = 0; k < 4; ++k)
+          ptx::mma_bf16_ts(tmem + t * 256 + 128, tmem + t * 256 + 64 + k * 8, at(dvh, v + k * 2048), kIdPV,
+                           (j > 0 || k > 0) ? 1u : 0u);
         return true;
       };
       // Per key tile j and Q tile t: the nope scores of tile j + 1 go out as soon as the
