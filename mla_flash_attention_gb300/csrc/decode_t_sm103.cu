@@ -535,8 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t o[8];
 #pragma unroll
             for (int x = 0; x < 4; ++x) {
-              o[2 * x] = ptx::e4m3x2_to_f16x2(c[x] & 0xFFFF);
-              o[2 * x + 1] = ptx::e4m3x2_to_f16x2(c[x] >> 16);
+              ptx::e4m3x4_to_f16x2x2(c[x], o[2 * x], o[2 * x + 1]);
             }
             *reinterpret_cast<uint4*>(wide + base + (((2 * h) ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
             *reinterpret_cast<uint4*>(wide + base + (((2 * h + 1) ^ (row & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);

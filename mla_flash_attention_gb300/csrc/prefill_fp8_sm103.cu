@@ -279,8 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t w[8];
 #pragma unroll
           for (int x = 0; x < 4; ++x) {
-            w[2 * x] = ptx::e4m3x2_to_f16x2(rw[x] & 0xFFFFu);
-            w[2 * x + 1] = ptx::e4m3x2_to_f16x2(rw[x] >> 16);
+            ptx::e4m3x4_to_f16x2x2(rw[x], w[2 * x], w[2 * x + 1]);
           }
           // columns 16g .. 16g+15 -> chunk g / 4, 16-byte groups 2(g%4), 2(g%4)+1 (swizzled)
           unsigned char* dst = sm + kOffVh + s * 2 * kKChunk + (g >> 2) * kKChunk + ct * 128;

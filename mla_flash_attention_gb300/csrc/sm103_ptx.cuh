@@ -486,12 +486,14 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t codes16) {
 }
 
 // Two e4m3 codes (low byte = first) -> packed f16x2, exactly (every e4m3 value is an f16).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes16) {
-  uint32_t r;
-  asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
-      : "=r"(r)
-      : "r"(codes16));
-  return r;
+// Four e4m3 codes (bytes 0..3 of `codes4`) -> two packed f16x2: bytes 0, 1 into `lo`,
+// bytes 2, 3 into `hi` (exact: every e4m3 value is an f16 value).  The register is split into
+// its 16-bit halves by one move, with no masking or narrowing of each pair of codes.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t codes4, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(codes4));
 }
 
 // Two floats -> packed f16x2 (round to nearest even); `lo` goes to the low half.
