@@ -104,25 +104,6 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity,
   return true;
 }
 
-// Barrier `id` over `n` threads (a multiple of 32) of the CTA.
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
-  asm volatile("barrier.cta.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
-// Barrier `id` over `n` threads that also returns the OR of every thread's `pred`.
-__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t n, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "barrier.cta.red.or.pred q, %2, %3, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(n)
-      : "memory");
-  return r != 0;
-}
-
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
@@ -134,14 +115,7 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
-// Bring a 2-D box into L2 ahead of its load (no shared memory, no completion signal).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c0, int c1) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(c0), "r"(c1)
-               : "memory");
-}
-
+// Bring a box into L2 ahead of its load (no shared memory, no completion signal).
 __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int c0, int c1, int c2) {
   asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global [%0, {%1, %2, %3}];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
